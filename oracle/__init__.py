@@ -1,0 +1,188 @@
+"""CPU oracle for the symmetric-window collectives -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s cpu_baseline /
+``--impl reference`` leg may import this package.  The product path (the CUDA
+library and its Python binding) never imports it, and the two share no code.
+
+The arithmetic lives in ``oracle.c`` (plain C, IEEE binary32 in source order,
+built with ``-O2 -ffp-contract=off -fno-fast-math``); this module only builds
+it with gcc, loads it with ctypes and marshals numpy arrays.
+
+Parity status: every function is pinned by ``tests/test_oracle.py`` to facts
+that do not come from this code, except ``rolling_le``, which is "parity
+unpinned" (the GIN reference page cites a rolling comparison without printing
+it; the reading taken is documented in ``oracle.c``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-std=c11",
+           "-Wall", "-Wextra", "-pthread"]
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc; host arch only)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *_CFLAGS, _SRC, "-o", tmp], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        sz = ctypes.c_size_t
+        i32 = ctypes.c_int
+        u64 = ctypes.c_uint64
+        lib.oracle_allreduce_sum_f32.argtypes = [i32, sz, P, sz, P]
+        lib.oracle_allreduce_sum_f32.restype = None
+        lib.oracle_allreduce_sum_bf16.argtypes = [i32, sz, P, sz, P]
+        lib.oracle_allreduce_sum_bf16.restype = None
+        lib.oracle_allreduce_sum_mt.argtypes = [i32, i32, sz, P, sz, P, i32]
+        lib.oracle_allreduce_sum_mt.restype = i32
+        lib.oracle_f32_to_bf16_rne.argtypes = [ctypes.c_float]
+        lib.oracle_f32_to_bf16_rne.restype = ctypes.c_uint16
+        lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f32.restype = ctypes.c_float
+        lib.oracle_f32_to_bf16_array.argtypes = [sz, P, P]
+        lib.oracle_f32_to_bf16_array.restype = None
+        lib.oracle_allgather.argtypes = [i32, sz, P, sz, P]
+        lib.oracle_allgather.restype = None
+        lib.oracle_put_signal_allgather.argtypes = [i32, sz, sz, sz, P, sz, P, P, P]
+        lib.oracle_put_signal_allgather.restype = None
+        lib.oracle_prefix_mismatch.argtypes = [sz, sz, sz, u64, P, P]
+        lib.oracle_prefix_mismatch.restype = u64
+        lib.oracle_rolling_le.argtypes = [u64, u64, i32]
+        lib.oracle_rolling_le.restype = i32
+        lib.oracle_read_bits.argtypes = [u64, i32]
+        lib.oracle_read_bits.restype = u64
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _rows(x: np.ndarray, dtype) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != dtype or x.ndim != 2:
+        raise TypeError(f"expected a 2-D {np.dtype(dtype).name} array (ranks x elements)")
+    return x
+
+
+def allreduce_sum_f32(x: np.ndarray) -> np.ndarray:
+    """x: (R, N) float32 -> y: (N,) float32, summed in rank order 0..R-1."""
+    x = _rows(x, np.float32)
+    R, n = x.shape
+    y = np.empty(n, np.float32)
+    if n:
+        _load().oracle_allreduce_sum_f32(R, n, _ptr(x), n, _ptr(y))
+    return y
+
+
+def allreduce_sum_bf16(x_bits: np.ndarray) -> np.ndarray:
+    """x_bits: (R, N) uint16 bf16 patterns -> (N,) uint16, fp32 accumulate, one RNE rounding."""
+    x = _rows(x_bits, np.uint16)
+    R, n = x.shape
+    y = np.empty(n, np.uint16)
+    if n:
+        _load().oracle_allreduce_sum_bf16(R, n, _ptr(x), n, _ptr(y))
+    return y
+
+
+def allreduce_sum_mt(x: np.ndarray, nthreads: int) -> tuple[np.ndarray, int]:
+    """Threaded driver of the same per-element routine (timing); returns (y, threads used)."""
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        is_bf16 = 0
+    elif x.dtype == np.uint16:
+        is_bf16 = 1
+    else:
+        raise TypeError("float32 or uint16 (bf16 bits) expected")
+    R, n = x.shape
+    y = np.empty(n, x.dtype)
+    used = _load().oracle_allreduce_sum_mt(is_bf16, R, n, _ptr(x), n, _ptr(y), int(nthreads))
+    return y, int(used)
+
+
+def f32_to_bf16(x: np.ndarray) -> np.ndarray:
+    """float32 array -> uint16 bf16 patterns, round to nearest even (NaN -> 0x7FC0)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    y = np.empty(x.size, np.uint16)
+    if x.size:
+        _load().oracle_f32_to_bf16_array(x.size, _ptr(x), _ptr(y))
+    return y
+
+
+def f32_to_bf16_scalar(v: float) -> int:
+    return int(_load().oracle_f32_to_bf16_rne(ctypes.c_float(v)))
+
+
+def bf16_to_f32(b: np.ndarray) -> np.ndarray:
+    """uint16 bf16 patterns -> float32 (exact widening)."""
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def allgather(x: np.ndarray) -> np.ndarray:
+    """x: (R, S) uint8 -> (R*S,) uint8: the recv buffer every rank holds."""
+    x = _rows(x, np.uint8)
+    R, S = x.shape
+    y = np.empty(R * S, np.uint8)
+    if y.size:
+        _load().oracle_allgather(R, S, _ptr(x), S, _ptr(y))
+    return y
+
+
+def put_signal_allgather(x: np.ndarray, chunk: int, batch: int):
+    """Sequential put+signal model. x: (R, S) uint8.
+
+    Returns (recv (R*S,) uint8, sig (R, R) uint64 indexed [peer, sender], cnt (R,) uint64).
+    """
+    x = _rows(x, np.uint8)
+    R, S = x.shape
+    if chunk < 1 or batch < 1:
+        raise ValueError("chunk and batch must be >= 1")
+    recv = np.empty(R * S, np.uint8)
+    sig = np.empty((R, R), np.uint64)
+    cnt = np.empty(R, np.uint64)
+    _load().oracle_put_signal_allgather(R, S, chunk, batch, _ptr(x), S, _ptr(recv),
+                                        _ptr(sig), _ptr(cnt))
+    return recv, sig, cnt
+
+
+def prefix_mismatch(src_q: np.ndarray, seg: np.ndarray, chunk: int, batch: int, k: int) -> int:
+    src_q = np.ascontiguousarray(src_q, dtype=np.uint8)
+    seg = np.ascontiguousarray(seg, dtype=np.uint8)
+    if src_q.size != seg.size:
+        raise ValueError("segment and source sizes differ")
+    return int(_load().oracle_prefix_mismatch(src_q.size, chunk, batch, k, _ptr(src_q), _ptr(seg)))
+
+
+def rolling_le(a: int, b: int, bits: int = 64) -> bool:
+    """PARITY UNPINNED reading of the rolling comparison (see oracle.c)."""
+    return bool(_load().oracle_rolling_le(a & (2**64 - 1), b & (2**64 - 1), bits))
+
+
+def read_bits(v: int, bits: int) -> int:
+    return int(_load().oracle_read_bits(v & (2**64 - 1), bits))

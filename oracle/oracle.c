@@ -1,0 +1,271 @@
+/*
+ * CPU oracle for symmetric-window collectives.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference
+ * leg may load this library.  The product path (the CUDA library under
+ * symmetric_memory_allreduce_gb300/) never calls it and shares no code with it.
+ *
+ * Every routine is the plain definition of what the method computes, written
+ * out element by element, with no blocking, fusion or reordering.  Build with
+ * -O2 -ffp-contract=off -fno-fast-math so that the compiler keeps IEEE binary32
+ * round-to-nearest-even adds in source order (on aarch64 GCC would otherwise be
+ * allowed to contract).
+ *
+ * Sources (web pages; cited by title and section):
+ *  [SYMEX]  "NCCL symmetric memory windows: examples 01_allreduce / 02_allgather"
+ *           (docs/examples/05_symmetric_memory walkthrough), Example 1 steps 4-6
+ *           and expected output; Example 2 buffers and expected output.
+ *  [GIN]    "NCCL Device API GIN reference": sections "put/get", "Signals and
+ *           Counters", "Signal methods", "Counter methods".
+ *  [GDA]    "GPUDirect Async deep dive" (GIN paper summary, section 4: ordering
+ *           of a batch of puts followed by one signal; section 5.3: batches of
+ *           at most 8 commands with one signalled request per batch).
+ *
+ * Parity status of each function is stated in its comment.  One function,
+ * oracle_rolling_le, is "parity unpinned": the page refers to a rolling
+ * comparison pseudo-code without printing it (see its comment).
+ */
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+#include <pthread.h>
+
+/* ------------------------------------------------------------------------ */
+/* AllReduce(sum), fp32.                                                    */
+/* [SYMEX] Example 1: every rank calls AllReduce(send, recv, count, float,  */
+/* sum); step 6 says each element equals the sum over all ranks.  The pages */
+/* do not fix an order; this oracle adds in rank order 0..R-1, one IEEE     */
+/* binary32 add at a time:                                                  */
+/*     y[i] = ((x[0][i] + x[1][i]) + x[2][i]) + ... + x[R-1][i]             */
+/* Every rank's recv buffer holds the same y.                               */
+/* x is R rows of ldx elements (row q = rank q's send buffer).              */
+/* Pins: rank-fill closed form R(R-1)/2; integer-valued data (exact in any  */
+/* order); brute force vs numpy float32 scalar adds; Higham error bound.    */
+/* ------------------------------------------------------------------------ */
+void oracle_allreduce_sum_f32(int R, size_t n, const float* x, size_t ldx, float* y)
+{
+    for (size_t i = 0; i < n; ++i) {
+        float acc = x[i];
+        for (int q = 1; q < R; ++q) {
+            acc = acc + x[(size_t)q * ldx + i];
+        }
+        y[i] = acc;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* bf16 <-> fp32.                                                           */
+/* bf16 is the top half of a binary32 pattern, so widening is exact:        */
+/*     bits32 = bits16 << 16.                                               */
+/* Narrowing rounds to nearest, ties to even (IEEE 754 roundTiesToEven),    */
+/* keeping Inf and mapping every NaN to the quiet NaN 0x7FC0.  With u the   */
+/* binary32 pattern, the kept half is u >> 16 and the dropped half is       */
+/* u & 0xFFFF; round up when the dropped half exceeds 0x8000, or equals it  */
+/* and the kept half is odd.  Adding 0x7FFF + (kept & 1) and shifting does  */
+/* exactly that, and a carry out of the mantissa correctly bumps the        */
+/* exponent (up to Inf for the largest finite values).                      */
+/* Pins: torch CPU conversion on stratified patterns; brute-force nearest   */
+/* neighbour in exact rationals; hand tie cases.                            */
+/* ------------------------------------------------------------------------ */
+float oracle_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+uint16_t oracle_f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u) {
+        return (uint16_t)0x7FC0u;                /* NaN */
+    }
+    uint32_t kept_lsb = (u >> 16) & 1u;
+    uint32_t r = u + 0x7FFFu + kept_lsb;
+    return (uint16_t)(r >> 16);
+}
+
+void oracle_f32_to_bf16_array(size_t n, const float* x, uint16_t* y)
+{
+    for (size_t i = 0; i < n; ++i) y[i] = oracle_f32_to_bf16_rne(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* AllReduce(sum), bf16 inputs, fp32 accumulation, one rounding.            */
+/* Each input is widened exactly, the fp32 sum is taken in rank order as in */
+/* the fp32 routine, and the result is rounded to bf16 once.                */
+/* Pins: numpy float32 rank-order loop + torch rounding; rank-fill.         */
+/* ------------------------------------------------------------------------ */
+void oracle_allreduce_sum_bf16(int R, size_t n, const uint16_t* x, size_t ldx, uint16_t* y)
+{
+    for (size_t i = 0; i < n; ++i) {
+        float acc = oracle_bf16_to_f32(x[i]);
+        for (int q = 1; q < R; ++q) {
+            acc = acc + oracle_bf16_to_f32(x[(size_t)q * ldx + i]);
+        }
+        y[i] = oracle_f32_to_bf16_rne(acc);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Threaded drivers (timing only).  The element range is split into equal   */
+/* contiguous parts, each handled by the same per-element routine above, so */
+/* results are identical to the single-threaded call.                       */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int R, is_bf16;
+    size_t lo, hi, ldx;
+    const void* x;
+    void* y;
+} oracle_job;
+
+static void* oracle_job_run(void* arg)
+{
+    oracle_job* j = (oracle_job*)arg;
+    size_t n = j->hi - j->lo;
+    if (j->is_bf16) {
+        oracle_allreduce_sum_bf16(j->R, n, (const uint16_t*)j->x + j->lo, j->ldx,
+                                  (uint16_t*)j->y + j->lo);
+    } else {
+        oracle_allreduce_sum_f32(j->R, n, (const float*)j->x + j->lo, j->ldx,
+                                 (float*)j->y + j->lo);
+    }
+    return NULL;
+}
+
+/* Returns the number of threads actually used. */
+int oracle_allreduce_sum_mt(int is_bf16, int R, size_t n, const void* x, size_t ldx,
+                            void* y, int nthreads)
+{
+    enum { MAXT = 256 };
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > MAXT) nthreads = MAXT;
+    if ((size_t)nthreads > n) nthreads = n > 0 ? (int)n : 1;
+    pthread_t th[MAXT];
+    oracle_job jobs[MAXT];
+    size_t per = (n + (size_t)nthreads - 1) / (size_t)nthreads;
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        size_t lo = (size_t)t * per, hi = lo + per;
+        if (lo > n) lo = n;
+        if (hi > n) hi = n;
+        jobs[t] = (oracle_job){R, is_bf16, lo, hi, ldx, x, y};
+        if (t == 0) continue;
+        if (pthread_create(&th[t], NULL, oracle_job_run, &jobs[t]) != 0) {
+            oracle_job_run(&jobs[t]);           /* run inline if no thread */
+            th[t] = (pthread_t)0;
+        } else {
+            ++started;
+        }
+    }
+    oracle_job_run(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t) {
+        if (th[t] != (pthread_t)0) pthread_join(th[t], NULL);
+    }
+    return started + 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* AllGather.                                                               */
+/* [SYMEX] Example 2: the recv buffer holds sendcount * nranks elements and */
+/* segment q holds rank q's send buffer:                                    */
+/*     recv_r[q*S + i] = send_q[i]   for every rank r, q and byte i < S.    */
+/* The result does not depend on r, so one buffer of R*S bytes is produced. */
+/* Pins: worked example (segment q = float(q)); numpy concatenation.        */
+/* ------------------------------------------------------------------------ */
+void oracle_allgather(int R, size_t S, const uint8_t* x, size_t ldx, uint8_t* y)
+{
+    for (int q = 0; q < R; ++q) {
+        for (size_t i = 0; i < S; ++i) {
+            y[(size_t)q * S + i] = x[(size_t)q * ldx + i];
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Chunked put + signal AllGather, sequential model.                        */
+/* [GIN] put: copy `bytes` from the source window at src_off to the peer's  */
+/* destination window at dst_off; the peer may be the caller (loopback).    */
+/* remoteAction SignalInc adds 1 to a signal on the peer; localAction       */
+/* CounterInc adds 1 to a counter on the caller once the source is read.    */
+/* [GDA] a batch of puts followed by one signal orders the batch.           */
+/* Model: for every sender q, every peer p (p = q included) and chunk k in  */
+/* ascending order, put chunk k of send_q to recv_p at q*S + k*chunk; after */
+/* each put, cnt[q] += 1; after every B-th chunk of a (q, p) stream and     */
+/* after its last chunk, sig[p*R + q] += 1 (signal id = sender rank).       */
+/* The last chunk may be short when chunk does not divide S.                */
+/* Outputs: recv (R*S bytes, identical for every p, so one buffer),         */
+/* sig (R*R), cnt (R).  The caller zeroes nothing; this routine does.       */
+/* Pins: closed forms sig = ceil(ceil(S/chunk)/B), cnt = R*ceil(S/chunk);   */
+/* recv equals the AllGather; prefix-visibility replay below.               */
+/* ------------------------------------------------------------------------ */
+void oracle_put_signal_allgather(int R, size_t S, size_t chunk, size_t B,
+                                 const uint8_t* x, size_t ldx,
+                                 uint8_t* recv, uint64_t* sig, uint64_t* cnt)
+{
+    memset(sig, 0, sizeof(uint64_t) * (size_t)R * (size_t)R);
+    memset(cnt, 0, sizeof(uint64_t) * (size_t)R);
+    size_t nchunks = (S + chunk - 1) / chunk;
+    for (int q = 0; q < R; ++q) {
+        for (int p = 0; p < R; ++p) {
+            size_t in_batch = 0;
+            for (size_t k = 0; k < nchunks; ++k) {
+                size_t off = k * chunk;
+                size_t len = (off + chunk <= S) ? chunk : S - off;
+                /* recv is shared by all p (the result does not depend on p);
+                 * every p writes the same bytes to the same place. */
+                memcpy(recv + (size_t)q * S + off, x + (size_t)q * ldx + off, len);
+                cnt[q] += 1;
+                in_batch += 1;
+                if (in_batch == B || k + 1 == nchunks) {
+                    sig[(size_t)p * R + q] += 1;
+                    in_batch = 0;
+                }
+            }
+        }
+    }
+}
+
+/* Prefix visibility, the strong-signal invariant of [GIN] "Signals and      */
+/* Counters" (a visible strong signal implies every earlier put on the same  */
+/* context to the same peer is visible): given a snapshot of recv_p's        */
+/* segment q and an observed signal value k, return the number of bytes of  */
+/* batches 0..k-1 (chunks 0..k*B-1) that differ from the source.  The        */
+/* expected answer for a correct implementation is 0.                        */
+uint64_t oracle_prefix_mismatch(size_t S, size_t chunk, size_t B, uint64_t k,
+                                const uint8_t* src_q, const uint8_t* seg)
+{
+    size_t covered = (size_t)k * B * chunk;
+    if (covered > S) covered = S;
+    uint64_t bad = 0;
+    for (size_t i = 0; i < covered; ++i) bad += (src_q[i] != seg[i]);
+    return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Rolling comparison.  PARITY UNPINNED (formula not printed on the page).  */
+/* [GIN] "Signals and Counters": signal and counter values are compared     */
+/* with a rolling rule so that x <= x+1 holds even across unsigned          */
+/* overflow; waitSignal(least, bits) returns once the low `bits` bits of    */
+/* the value are rolling-greater-or-equal to `least`.  Reading taken: with  */
+/* m = 2^bits - 1 and d = (b - a) mod 2^bits, a <= b iff d < 2^(bits-1).    */
+/* ------------------------------------------------------------------------ */
+int oracle_rolling_le(uint64_t a, uint64_t b, int bits)
+{
+    if (bits < 1) bits = 1;
+    if (bits > 64) bits = 64;
+    uint64_t m = (bits == 64) ? ~(uint64_t)0 : (((uint64_t)1 << bits) - 1);
+    uint64_t d = (b - a) & m;
+    uint64_t half = (uint64_t)1 << (bits - 1);
+    return d < half;
+}
+
+/* readSignal / readCounter: the low `bits` bits of the value. */
+uint64_t oracle_read_bits(uint64_t v, int bits)
+{
+    if (bits >= 64) return v;
+    if (bits < 1) return 0;
+    return v & (((uint64_t)1 << bits) - 1);
+}

@@ -1,0 +1,314 @@
+"""Pins for the CPU oracle: facts that do not come from the oracle's own code.
+
+Each test names what it pins and where the fact comes from: the pages' worked
+examples (tests/golden/), closed forms, brute force written independently
+(numpy float32 scalar adds, exact rationals), or a library routine that
+computes the same definition (torch's round-to-nearest-even bf16 conversion).
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        line = [l for l in f if l.strip() and not l.startswith("#")][0]
+    return dict(kv.split("=") for kv in line.split())
+
+
+def _seq_sum_np(x):
+    """Independent rank-order sum: numpy float32 scalar adds, one at a time."""
+    R, n = x.shape
+    y = np.empty(n, np.float32)
+    for i in range(n):
+        acc = np.float32(x[0, i])
+        for q in range(1, R):
+            acc = np.float32(acc + np.float32(x[q, i]))
+        y[i] = acc
+    return y
+
+
+# ---------------------------------------------------------------- AllReduce fp32
+
+def test_allreduce_worked_example(oracle):
+    """Example 1 of the symmetric-memory guide: 4 ranks filled with their rank -> 6.0."""
+    g = _golden("allreduce_rankfill.txt")
+    R, n = int(g["ranks"]), int(g["count"])
+    x = np.repeat(np.arange(R, dtype=np.float32)[:, None], n, axis=1)
+    y = oracle.allreduce_sum_f32(x)
+    assert y.shape == (n,)
+    assert np.all(np.abs(y - float(g["expected"])) <= float(g["tolerance"]))
+    assert np.all(y == np.float32(6.0))            # exact: small integers
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 8, 16, 64])
+def test_allreduce_rankfill_closed_form(oracle, R):
+    """Closed form of the same example for other rank counts: R(R-1)/2, exact in fp32."""
+    x = np.repeat(np.arange(R, dtype=np.float32)[:, None], 37, axis=1)
+    assert np.all(oracle.allreduce_sum_f32(x) == np.float32(R * (R - 1) // 2))
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8, 16])
+@pytest.mark.parametrize("n", [0, 1, 7, 33, 1000])
+def test_allreduce_integer_data_exact(oracle, R, n):
+    """Integer-valued data |x| <= 2^10: every order is exact, so y is the integer sum."""
+    rng = np.random.default_rng(1000 * R + n)
+    xi = rng.integers(-1024, 1025, size=(R, n))
+    y = oracle.allreduce_sum_f32(xi.astype(np.float32))
+    assert np.array_equal(y.astype(np.int64), xi.sum(axis=0))
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("n", [0, 1, 3, 4, 5, 8, 9, 31, 33, 200])
+def test_allreduce_brute_force_rank_order(oracle, R, n):
+    """Bit-exact against an independent rank-order loop of numpy float32 scalar adds."""
+    rng = np.random.default_rng(7 * R + n)
+    x = (rng.standard_normal((R, n)) * rng.choice([1e-3, 1.0, 1e3], size=(R, n))).astype(np.float32)
+    y = oracle.allreduce_sum_f32(x)
+    assert np.array_equal(y.view(np.uint32), _seq_sum_np(x).view(np.uint32))
+
+
+def test_allreduce_rank_order_is_pinned(oracle):
+    """Order-sensitive cases: forward rank order differs from reverse and from a pairwise tree."""
+    # forward: (1 + 1e8) + -1e8 = 0 ; reverse: (-1e8 + 1e8) + 1 = 1
+    x = np.array([[1.0], [1e8], [-1e8]], np.float32)
+    assert oracle.allreduce_sum_f32(x)[0] == np.float32(0.0)
+    # forward: ((1e8 + 1) - 1e8) + 1 = 1 ; tree: (1e8 + 1) + (-1e8 + 1) = 0
+    x = np.array([[1e8], [1.0], [-1e8], [1.0]], np.float32)
+    assert oracle.allreduce_sum_f32(x)[0] == np.float32(1.0)
+
+
+def test_allreduce_error_bound(oracle):
+    """Recursive summation bound: |y - exact| <= (R-1) u sum|x| / (1 - (R-1) u), u = 2^-24."""
+    rng = np.random.default_rng(3)
+    R, n = 16, 4096
+    x = rng.standard_normal((R, n)).astype(np.float32)
+    y = oracle.allreduce_sum_f32(x).astype(np.float64)
+    exact = x.astype(np.float64).sum(axis=0)   # fp64 sum of 16 floats: error << fp32 ulp
+    u = 2.0 ** -24
+    g = (R - 1) * u / (1 - (R - 1) * u)
+    assert np.all(np.abs(y - exact) <= g * np.abs(x.astype(np.float64)).sum(axis=0) + 1e-30)
+
+
+def test_allreduce_special_values(oracle):
+    """R=1 copies bits (including -0.0 and subnormals); subnormal sums are not flushed."""
+    tiny = np.float32(1e-45)     # smallest subnormal
+    x = np.array([[-0.0, tiny, 3.0, -np.inf, np.float32(1e-40)]], np.float32)
+    assert np.array_equal(oracle.allreduce_sum_f32(x).view(np.uint32), x[0].view(np.uint32))
+    x2 = np.array([[tiny, 1e-40], [tiny, 1e-40]], np.float32)
+    y2 = oracle.allreduce_sum_f32(x2)
+    assert y2[0:1].view(np.uint32)[0] == 2        # 2 x smallest subnormal, not flushed
+    assert y2[1] == np.float32(1e-40) + np.float32(1e-40)
+    x3 = np.array([[np.inf], [-np.inf]], np.float32)
+    assert np.isnan(oracle.allreduce_sum_f32(x3)[0])
+
+
+def test_allreduce_threaded_identical(oracle):
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((8, 100_003)).astype(np.float32)
+    y1 = oracle.allreduce_sum_f32(x)
+    y4, used = oracle.allreduce_sum_mt(x, 4)
+    assert used == 4
+    assert np.array_equal(y1.view(np.uint32), y4.view(np.uint32))
+    xb = oracle.f32_to_bf16(x).reshape(x.shape)
+    b1 = oracle.allreduce_sum_bf16(xb)
+    b3, _ = oracle.allreduce_sum_mt(xb, 3)
+    assert np.array_equal(b1, b3)
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def _torch_bf16_bits(f32):
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(f32, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_bf16_hand_cases(oracle):
+    """Hand cases from the roundTiesToEven definition."""
+    cases = {
+        0x3F800000: 0x3F80,   # 1.0 exact
+        0x3F808000: 0x3F80,   # tie, kept half even -> stays
+        0x3F818000: 0x3F82,   # tie, kept half odd -> rounds up to even
+        0x3F808001: 0x3F81,   # just above the tie
+        0x3F807FFF: 0x3F80,   # just below the tie
+        0xBF818000: 0xBF82,   # negative tie (magnitude rounds to even)
+        0x7F7FFFFF: 0x7F80,   # largest float rounds to +Inf
+        0x7F800000: 0x7F80,   # +Inf
+        0xFF800000: 0xFF80,   # -Inf
+        0x00000001: 0x0000,   # smallest subnormal rounds to +0
+        0x00008000: 0x0000,   # subnormal tie to even (0)
+        0x00018000: 0x0002,   # subnormal tie to even (2)
+        0x80000000: 0x8000,   # -0
+        0x7FC00001: 0x7FC0,   # NaN -> canonical quiet NaN
+        0xFFFFFFFF: 0x7FC0,
+    }
+    for u, b in cases.items():
+        f = np.array([u], np.uint32).view(np.float32)[0]
+        assert oracle.f32_to_bf16_scalar(float(f)) == b, hex(u)
+        assert oracle.f32_to_bf16(np.array([f]))[0] == b, hex(u)
+
+
+def test_bf16_rounding_matches_torch_stratified(oracle):
+    """Every upper half x {0, 1, 0x7FFF, 0x8000, 0x8001, 0xFFFF} low halves, plus 2^20 random."""
+    hi = np.arange(1 << 16, dtype=np.uint32) << 16
+    lows = np.array([0, 1, 0x7FFF, 0x8000, 0x8001, 0xFFFF], np.uint32)
+    u = (hi[:, None] | lows[None, :]).ravel()
+    rng = np.random.default_rng(5)
+    u = np.concatenate([u, rng.integers(0, 2**32, size=1 << 20, dtype=np.uint64).astype(np.uint32)])
+    f = u.view(np.float32)
+    finite_or_inf = ~np.isnan(f)
+    ours = oracle.f32_to_bf16(f)
+    ref = _torch_bf16_bits(f)
+    assert np.array_equal(ours[finite_or_inf], ref[finite_or_inf])
+    assert np.all(ours[~finite_or_inf] == 0x7FC0)
+
+
+def _bf16_value(bits):
+    s = -1 if bits & 0x8000 else 1
+    e = (bits >> 7) & 0xFF
+    m = bits & 0x7F
+    if e == 0:
+        return s * Fraction(m, 1 << 7) * Fraction(1, 2 ** 126)
+    return s * (1 + Fraction(m, 1 << 7)) * (Fraction(2) ** (e - 127))
+
+
+def test_bf16_rounding_brute_force_nearest(oracle):
+    """Exact rationals: pick the nearer of the two bf16 neighbours, ties to even mantissa."""
+    rng = np.random.default_rng(9)
+    u = rng.integers(0, 2**32, size=3000, dtype=np.uint64).astype(np.uint32)
+    u = u[(u & 0x7F800000) != 0x7F800000]             # finite only
+    u = u[(u & 0x7FFFFFFF) < 0x7F7F8000]              # neighbours stay finite
+    for word in u:
+        f = np.array([word], np.uint32).view(np.float32)[0]
+        exact = Fraction(float(f))
+        lo = int(word >> 16)                          # truncation toward zero
+        hi = lo + 1
+        dlo = abs(exact - _bf16_value(lo))
+        dhi = abs(exact - _bf16_value(hi))
+        want = lo if dlo < dhi else hi if dhi < dlo else (lo if lo % 2 == 0 else hi)
+        assert oracle.f32_to_bf16(np.array([f]))[0] == want, hex(int(word))
+
+
+def test_bf16_widen_exact(oracle):
+    b = np.arange(1 << 16, dtype=np.uint16)
+    f = oracle.bf16_to_f32(b)
+    back = oracle.f32_to_bf16(f)
+    nan = np.isnan(f)
+    assert np.array_equal(back[~nan], b[~nan])
+
+
+# ---------------------------------------------------------------- AllReduce bf16
+
+def test_allreduce_bf16_worked_example(oracle):
+    R, n = 4, 4096
+    x = np.repeat(np.arange(R, dtype=np.float32)[:, None], n, axis=1)
+    y = oracle.allreduce_sum_bf16(oracle.f32_to_bf16(x).reshape(R, n))
+    assert np.all(y == 0x40C0)    # 6.0 in bf16
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 8])
+def test_allreduce_bf16_brute_force(oracle, R):
+    """Widen exactly, add float32 scalars in rank order, round once (torch RNE)."""
+    rng = np.random.default_rng(40 + R)
+    n = 257
+    x = _torch_bf16_bits(rng.uniform(-4, 4, size=R * n).astype(np.float32)).reshape(R, n)
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    want = _torch_bf16_bits(_seq_sum_np(xf))
+    assert np.array_equal(oracle.allreduce_sum_bf16(x), want)
+
+
+def test_allreduce_bf16_single_rounding(oracle):
+    """One rounding of the fp32 sum, not a rounding after every add."""
+    # 1 + 2^-8 + 2^-8: per-add rounding gives 1.0 (ties to even twice); one rounding gives 1+2^-7
+    one, e = 0x3F80, 0x3B80                     # 1.0 and 2^-8 in bf16
+    x = np.array([[one], [e], [e]], np.uint16)
+    assert oracle.allreduce_sum_bf16(x)[0] == 0x3F81
+
+
+# ---------------------------------------------------------------- AllGather
+
+def test_allgather_worked_example(oracle):
+    """Example 2 of the symmetric-memory guide: segment q holds q.0 on every rank."""
+    g = _golden("allgather_rankfill.txt")
+    R, n = int(g["ranks"]), int(g["count"])
+    segs = [float(v) for v in g["segments"].split(",")]
+    x = np.repeat(np.arange(R, dtype=np.float32)[:, None], n, axis=1)
+    y = oracle.allgather(x.view(np.uint8)).view(np.float32)
+    assert y.size == R * n
+    for q in range(R):
+        assert np.all(y[q * n:(q + 1) * n] == segs[q])
+
+
+@pytest.mark.parametrize("R,S", [(1, 5), (3, 17), (16, 4096), (4, 0)])
+def test_allgather_random_bytes(oracle, R, S):
+    rng = np.random.default_rng(R * 100 + S)
+    x = rng.integers(0, 256, size=(R, S), dtype=np.uint8)
+    assert np.array_equal(oracle.allgather(x), np.concatenate(list(x)) if S else np.zeros(0, np.uint8))
+
+
+# ---------------------------------------------------------------- put + signal
+
+@pytest.mark.parametrize("R,S,chunk,B", [(16, 1 << 16, 1 << 12, 8), (4, 1000, 64, 3), (3, 64, 64, 1),
+                                         (2, 4096, 512, 8), (5, 4095, 512, 100)])
+def test_put_signal_model_closed_forms(oracle, R, S, chunk, B):
+    rng = np.random.default_rng(S + R)
+    x = rng.integers(0, 256, size=(R, S), dtype=np.uint8)
+    recv, sig, cnt = oracle.put_signal_allgather(x, chunk, B)
+    nchunks = -(-S // chunk)
+    assert np.array_equal(recv, np.concatenate(list(x)))
+    assert np.all(sig == -(-nchunks // B))
+    assert np.all(cnt == R * nchunks)
+
+
+def test_put_signal_model_config5_counts(oracle):
+    """R=16, 32 MiB in 64 KiB chunks (512 chunks), 8 chunks per signal -> 64 signals per pair."""
+    R, chunk, B = 16, 64 << 10, 8
+    S = 2 * chunk * B + chunk // 2          # small stand-in with a short last chunk
+    x = np.tile(np.arange(R, dtype=np.uint8)[:, None], (1, S))
+    recv, sig, cnt = oracle.put_signal_allgather(x, chunk, B)
+    for q in range(R):                      # byte fill: segment q is all q
+        assert np.all(recv[q * S:(q + 1) * S] == q)
+    assert np.all(sig == 3)                 # 17 chunks in batches of 8 -> 8, 8, 1
+    assert np.all(cnt == R * 17)            # one count per put, R peers per sender
+
+
+def test_prefix_mismatch(oracle):
+    rng = np.random.default_rng(1)
+    chunk, B, S = 256, 2, 256 * 7
+    src = rng.integers(0, 256, S, dtype=np.uint8)
+    seg = src.copy()
+    assert oracle.prefix_mismatch(src, seg, chunk, B, 4) == 0
+    seg[3 * chunk + 5] ^= 0xFF                # inside batch 1 (chunks 2-3)
+    assert oracle.prefix_mismatch(src, seg, chunk, B, 1) == 0
+    assert oracle.prefix_mismatch(src, seg, chunk, B, 2) == 1
+    assert oracle.prefix_mismatch(src, seg, chunk, B, 99) == 1
+
+
+# ---------------------------------------------------------------- rolling compare (unpinned)
+
+def test_rolling_le_truth_table(oracle):
+    """Only the page's stated property is pinned: x <= x and x <= x+1 across wrap."""
+    M = 2**64 - 1
+    assert oracle.rolling_le(0, 0)
+    assert not oracle.rolling_le(5, 4)
+    assert oracle.rolling_le(4, 5)
+    assert oracle.rolling_le(M, 0)                  # x <= x+1 across overflow
+    assert not oracle.rolling_le(0, M)
+    assert not oracle.rolling_le(0, 2**63)          # reading: half-range is "behind"
+    assert oracle.rolling_le(0, 2**63 - 1)
+    m56 = 2**56 - 1
+    assert oracle.rolling_le(m56, 0, 56)            # 56-bit counters wrap at 2^56
+    assert oracle.rolling_le(m56, 2**56, 56)        # high bits ignored
+    assert not oracle.rolling_le(1, 0, 56)
+    for x in [0, 1, 2**32, 2**63, M]:
+        assert oracle.rolling_le(x, x + 1)
+        assert oracle.rolling_le(x, x)
+    assert oracle.read_bits(2**60 + 5, 56) == 5
+    assert oracle.read_bits(M, 64) == M
