@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark: symmetric-window AllReduce(sum), R=8 rank windows of 256 MiB fp32
+(67,108,864 elements per rank, seeded U(-1,1)), two-shot, on one GB300.
+
+One step = one sym_allreduce call over the whole workload (inputs resident in
+HBM).  Prints ONE JSON line (rank 0):
+
+  value      algbw = bytes per rank / step time, summed over replicas (GB/s)
+  roofline   HBM-bound: compulsory bytes of the dominant kernel per launch
+             (read R*S + write R*S) / its average CUDA-event duration, against
+             the measured copy bandwidth; traffic = ncu DRAM bytes per launch
+  e2e        the same metric through the C ABI with pinned HOST buffers: every
+             step copies the R inputs in and the R results out
+  cpu_baseline  the CPU oracle (test infrastructure) timed on a bounded sample
+
+  --impl reference  times the CPU oracle as the reference arm (rank 0 only).
+
+Multi-GPU (torchrun, --gpus N): every rank runs an independent replica of the
+one-GPU emulation (no data-path collective); barrier + max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "AllReduce algbw GB/s and HBM GB/s (% of peak) at R=8, 256 MB/rank fp32, 1 GB300"
+R_DEFAULT, N_DEFAULT = 8, 1 << 26
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "twoshot_st_f32_R8_traffic.json")
+KERNEL_SRC = os.path.join(ROOT, "symmetric_memory_allreduce_gb300", "csrc", "allreduce.cu")
+
+
+# ----------------------------------------------------------------- pure helpers (CPU-testable)
+
+def algo_bytes(algo: str, R: int, S: int) -> dict:
+    """Per-launch byte models of one AllReduce of S bytes per rank over R windows.
+
+    compulsory: the HBM bytes the emulation cannot avoid (each input read once,
+    each output written once).  logical: bytes the algorithm's loads and stores
+    name (repeated reads of one line by several rank-slots counted each time).
+    """
+    logical = {"oneshot": R * (R + 1) * S, "twoshot": 2 * R * S,
+               "twoshot_pull": (3 * R - 1) * S, "twoshot_split": (3 * R - 1) * S}[algo]
+    return {"compulsory": 2 * R * S, "logical": logical}
+
+
+def measured_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(R: int, S: int) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("source_sha256") != kernel_source_hash():
+        return None
+    per_byte = float(t["dram_bytes_per_launch"]) / float(t["bytes_per_rank"])
+    return per_byte * S if int(t["R"]) == R else None
+
+
+def percentile(xs, q):
+    xs = sorted(xs)
+    if not xs:
+        return float("nan")
+    k = (len(xs) - 1) * q
+    lo, hi = int(k), min(int(k) + 1, len(xs) - 1)
+    return xs[lo] + (xs[hi] - xs[lo]) * (k - lo)
+
+
+def summarize_clocks(samples: list[dict], max_mhz: float | None) -> dict:
+    reasons = set()
+    for s in samples:
+        reasons.update(s.get("reasons", []))
+    busy = [s["sm_mhz"] for s in samples if "gpu_idle" not in s.get("reasons", [])] or \
+           [s["sm_mhz"] for s in samples]
+    return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max_mhz,
+            "reasons": sorted(reasons), "samples": len(samples)}
+
+
+def max_over_ranks(value: float) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- clocks (read-only NVML)
+
+_REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+                0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+                0x100: "display_clock_setting"}
+
+
+class ClockSampler(threading.Thread):
+    """Samples SM clock and clock-event reasons every ~20 ms (reads only)."""
+
+    def __init__(self, pci_bus_id: str | None):
+        super().__init__(daemon=True)
+        self.samples: list[dict] = []
+        self.max_mhz = None
+        self._halt = threading.Event()
+        self._nvml = None
+        self._h = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit")
+            h = ctypes.c_void_p()
+            ok = False
+            if pci_bus_id:
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) == 0
+            if not ok:
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) == 0
+            if not ok:
+                raise OSError("nvml handle")
+            m = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = float(m.value)
+            self._nvml, self._h = nv, h
+        except OSError:
+            self._nvml = None
+
+    def _sample(self):
+        nv, h = self._nvml, self._h
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) != 0:
+            return
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        reasons = []
+        if fn(h, ctypes.byref(rs)) == 0:
+            reasons = [n for b, n in _REASON_BITS.items() if rs.value & b]
+        self.samples.append({"t": time.time(), "sm_mhz": float(mhz.value), "reasons": reasons})
+
+    def run(self):
+        if self._nvml is None:
+            return
+        while not self._halt.is_set():
+            self._sample()
+            time.sleep(0.02)
+
+    def stop(self):
+        self._halt.set()
+        self.join(timeout=2)
+
+    def window(self, t0: float, t1: float) -> list[dict]:
+        return [s for s in self.samples if t0 <= s["t"] <= t1]
+
+
+def nvidia_smi_clocks() -> dict | None:
+    """One-shot fallback when NVML is not loadable."""
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                             timeout=10).stdout.split("\n")[0].split(",")
+        return {"sm_mhz": float(out[0]), "sm_max_mhz": float(out[1]), "reasons": [],
+                "samples": 1, "note": "nvidia-smi after the timed region"}
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- CPU oracle legs
+
+def cpu_oracle_rate(x_sample, budget_s: float) -> dict:
+    """Times the oracle (test infrastructure) over a bounded sample; returns GB/s of algbw."""
+    import oracle
+
+    oracle.build()
+    R, n = x_sample.shape
+    nthreads = os.cpu_count() or 1
+    passes, used = 0, 1
+    t0 = time.perf_counter()
+    while True:
+        _, used = oracle.allreduce_sum_mt(x_sample, nthreads)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    S = n * x_sample.itemsize
+    return {"value": S * passes / el / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
+            "sample": f"R={R} x {n} fp32 elements per rank (first {S >> 20} MiB of each rank's "
+                      f"256 MiB input), {passes} passes in {el:.1f} s, {used} threads",
+            "seconds_per_pass": el / passes}
+
+
+def run_reference(args) -> int:
+    """The reference arm: the CPU oracle, rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    R = R_DEFAULT
+    n_sample = 1 << 22            # 16 MiB per rank: one pass ~10-100 ms on a host
+    x = wl.uniform_f32(3, R, n_sample)
+    import oracle
+
+    oracle.build()
+    nthreads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.allreduce_sum_mt(x, nthreads)
+    times = []
+    used = 1
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _, used = oracle.allreduce_sum_mt(x, nthreads)
+        times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    S = n_sample * 4
+    value = S / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded U(-1,1) fp32, PCG64)",
+            "config": _config(R, N_DEFAULT, "oracle (CPU, rank order)"),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": used, "kind": "oracle",
+                             "sample": f"R={R} x {n_sample} fp32 elements per rank per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(R, n, algo):
+    return {"workload": f"AllReduce(sum) R={R} rank windows x {n} fp32 elements "
+                        f"({n * 4 >> 20} MiB) per rank, seeded U(-1,1)",
+            "R": R, "count_per_rank": n, "bytes_per_rank": n * 4, "algo": algo,
+            "l2": "inputs 2 GiB > 126 MiB L2 (no flush needed)", "parallelism": "replicas"}
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args) -> int:
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import symmetric_memory_allreduce_gb300 as sm
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    sm.load()
+    R, n = args.ranks, args.count
+    S = n * 4
+    x = wl.uniform_f32(3, R, n) if n == N_DEFAULT else wl.normal_f32(4, R, n)
+    send, recv = sm.Window(R, S), sm.Window(R, S)
+    stream = torch.cuda.current_stream()
+    for r in range(R):
+        send.write(r, x[r])
+    stream.synchronize()
+
+    def step():
+        sm.sym_allreduce(send, recv, n, "f32", "sum", args.algo)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if sm.sym_stream_status() != sm.SYM_OK:
+        raise RuntimeError("warm-up reported a device status: " + sm.sym_last_error())
+
+    props = torch.cuda.get_device_properties(local)
+    try:
+        bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    except AttributeError:
+        bus = None
+    sampler = ClockSampler(bus)
+    sampler.start()
+    time.sleep(0.05)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = sm.sym_launch_count()
+    w0 = time.time()
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier()
+    launches = sm.sym_launch_count() - launches0
+    sampler.stop()
+    if sm.sym_stream_status() != sm.SYM_OK:
+        raise RuntimeError("timed region reported a device status: " + sm.sym_last_error())
+    total_ms = t_all0.elapsed_time(t_all1)
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kern_ms = sum(per) / len(per)
+    total_ms = max_over_ranks(total_ms)
+    ms_per_step = total_ms / args.steps
+    value = world * S / (ms_per_step * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peak()
+    bytes_model = algo_bytes(args.algo if args.algo != "auto" else
+                             sm.sym_allreduce_algo(send, n, "f32"), R, S)
+    achieved = bytes_model["compulsory"] / (kern_ms * 1e-3) / 1e9
+    clk_samples = sampler.window(w0, w1)
+    clocks = summarize_clocks(clk_samples, sampler.max_mhz) if clk_samples else nvidia_smi_clocks()
+
+    # e2e: pinned host buffers through the C ABI, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, args.e2e_steps))
+        h_in = torch.empty((R, S), dtype=torch.uint8, pin_memory=True)
+        h_in.numpy()[:] = x.view(np.uint8)
+        h_out = torch.empty((R, S), dtype=torch.uint8, pin_memory=True)
+        ptr_in, ptr_out = h_in.data_ptr(), h_out.data_ptr()
+
+        def e2e_step():
+            for r in range(R):
+                send.write(r, (ptr_in + r * S, S))
+            step()
+            for r in range(R):
+                recv.read(r, (ptr_out + r * S, S))
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
+        e2e = {"value": world * S / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": R * S, "d2h_bytes_per_step": R * S, "steps": e2e_steps,
+               "ms_per_step": e_ms}
+        del h_in, h_out
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_rate(np.ascontiguousarray(x[:, : min(n, 1 << 24)]), args.cpu_seconds)
+
+    traffic = recorded_traffic(R, S)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded U(-1,1) fp32 per rank, numpy PCG64)",
+        "config": _config(R, n, args.algo),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "k_twoshot_st<F32T,8,2>" if args.algo in ("twoshot", "auto")
+                     else args.algo, "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "bytes_per_launch": bytes_model["compulsory"],
+                     "kernel_ms": kern_ms, "kernel_ms_p10": percentile(per, 0.1),
+                     "kernel_ms_p90": percentile(per, 0.9)},
+        "hbm_gbs": achieved, "hbm_pct_of_peak": 100.0 * achieved / peak,
+        "logical_gbs": bytes_model["logical"] / (kern_ms * 1e-3) / 1e9,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    send.free()
+    recv.free()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--algo", default="twoshot",
+                    choices=["auto", "oneshot", "twoshot", "twoshot_pull", "twoshot_split"])
+    ap.add_argument("--ranks", type=int, default=R_DEFAULT)
+    ap.add_argument("--count", type=int, default=N_DEFAULT)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args(argv)
+    a.warmup = max(a.warmup, 3)          # at least three untimed warm-up steps
+    return a
+
+
+def main(argv=None) -> int:
+    args = parse(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,505 @@
+// AllGather, one-sided put with signal/counter actions, and bounded waits.
+//
+// [SYMEX] Example 2: recv_r holds sendcount*R elements, segment q = rank q's
+// send buffer.  [GIN] put(peer, dstWnd, dstOffset, srcWnd, srcOffset, bytes,
+// remoteAction = SignalInc, localAction = CounterInc); a strong signal's
+// visibility implies every earlier put on the same context to the same peer
+// is visible; signals and counters are 64-bit values under 32-bit IDs,
+// counters read through 56 bits; waitSignal(least, bits) uses a rolling
+// comparison.  [GDA] section 4: a batch of puts closed by one signal orders
+// the batch without a global fence; section 5.1: completion flags use
+// release stores and an acquire spin with a short sleep.
+//
+// On one GPU a "put to peer p" is a copy into rank p's part of the
+// destination window, and remote visibility is device-scope visibility, so
+// every release/acquire here is .gpu scope (sys scope would also drain the
+// host path and is never needed: [GDA] section 5.2 notes its cost).
+#include <cstdio>
+
+#include "symar_internal.cuh"
+
+namespace symar {
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyU = 4;
+constexpr int kPutThreads = 512;
+constexpr int kPutU = 4;
+
+// ----------------------------------------------------------------- AllGather (copy)
+
+struct AgArgs {
+    const char* send;
+    char* recv;
+    size_t sstride, rstride;
+    int R;
+    size_t S;                 // bytes per rank segment
+    size_t nvec;              // S / 16 (vector path)
+    uint32_t tiles;           // tiles per segment
+};
+
+// Each item reads one tile of segment q once and stores it to all R ranks.
+__global__ void __launch_bounds__(kCopyThreads) k_allgather_copy(AgArgs a) {
+    constexpr size_t TILEV = (size_t)kCopyThreads * kCopyU;
+    const uint32_t items = (uint32_t)a.R * a.tiles;
+    for (uint32_t w = blockIdx.x; w < items; w += gridDim.x) {
+        const uint32_t t = w / (uint32_t)a.R, q = w - t * (uint32_t)a.R;
+        const char* src = a.send + (size_t)q * a.sstride;
+        const size_t seg = (size_t)q * a.S;
+        uint4 v[kCopyU];
+        size_t idx[kCopyU];
+#pragma unroll
+        for (int k = 0; k < kCopyU; ++k) {
+            idx[k] = (size_t)t * TILEV + threadIdx.x + (size_t)k * kCopyThreads;
+            if (idx[k] < a.nvec) v[k] = __ldcs(reinterpret_cast<const uint4*>(src + idx[k] * 16));
+        }
+        for (int r = 0; r < a.R; ++r) {
+            char* dst = a.recv + (size_t)r * a.rstride + seg;
+#pragma unroll
+            for (int k = 0; k < kCopyU; ++k)
+                if (idx[k] < a.nvec) __stcs(reinterpret_cast<uint4*>(dst + idx[k] * 16), v[k]);
+        }
+    }
+}
+
+// Byte-granular fallback when S is not a multiple of 16.
+__global__ void k_allgather_bytes(AgArgs a) {
+    const size_t total = (size_t)a.R * a.S;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t q = i / a.S, off = i - q * a.S;
+        const unsigned char b = (unsigned char)a.send[q * a.sstride + off];
+        for (int r = 0; r < a.R; ++r) a.recv[(size_t)r * a.rstride + q * a.S + off] = (char)b;
+    }
+}
+
+// ----------------------------------------------------------------- copy helper
+
+// Block-wide copy of [lo, hi) bytes from src to dst (same offsets).
+template <int THREADS, int U>
+__device__ __forceinline__ void block_copy(const char* src, char* dst, size_t lo, size_t hi,
+                                           bool vec) {
+    if (vec) {
+        const size_t v0 = lo / 16, v1 = hi / 16;
+        for (size_t base = v0; base < v1; base += (size_t)THREADS * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const size_t i = base + threadIdx.x + (size_t)k * THREADS;
+                if (i < v1) v[k] = __ldcs(reinterpret_cast<const uint4*>(src + i * 16));
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const size_t i = base + threadIdx.x + (size_t)k * THREADS;
+                if (i < v1) __stcs(reinterpret_cast<uint4*>(dst + i * 16), v[k]);
+            }
+        }
+    } else {
+        for (size_t i = lo + threadIdx.x; i < hi; i += THREADS) dst[i] = src[i];
+    }
+}
+
+// ----------------------------------------------------------------- put + signal AllGather
+
+struct PsArgs {
+    const char* send;
+    char* recv;
+    size_t sstride, rstride;
+    int R;
+    size_t S, chunk;
+    uint32_t B, nchunks, nbatches;
+    uint64_t* sig;            // recv window signals [R][nsig]
+    uint32_t nsig;
+    uint64_t* cnt;            // send window counters [R][ncnt]
+    uint32_t ncnt;
+    uint64_t* mismatch;       // optional prefix-visibility check
+    uint32_t nproducers;      // CTAs [0, nproducers) put; the rest only receive
+    uint32_t* status;
+    uint64_t timeout_ns;
+    int vec;
+};
+
+__device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* s_red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    uint64_t t = 0;
+    if (threadIdx.x == 0)
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += s_red[i];
+    __syncthreads();
+    return t;
+}
+
+__global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) {
+    __shared__ uint64_t s_v[2];
+    __shared__ uint64_t s_red[kPutThreads / 32];
+    const uint32_t R = (uint32_t)a.R, pairs = R * R;
+    // ---- senders: one CTA streams all batches of a (q -> p) pair in order
+    if (blockIdx.x < a.nproducers) {
+        for (uint32_t pr = blockIdx.x; pr < pairs; pr += a.nproducers) {
+            const uint32_t p = pr / R, q = pr - p * R;
+            const char* src = a.send + (size_t)q * a.sstride;
+            char* dst = a.recv + (size_t)p * a.rstride + (size_t)q * a.S;
+            for (uint32_t b = 0; b < a.nbatches; ++b) {
+                const uint32_t k0 = b * a.B, k1 = min(k0 + a.B, a.nchunks);
+                const size_t lo = (size_t)k0 * a.chunk, hi = min((size_t)k1 * a.chunk, a.S);
+                block_copy<kPutThreads, kPutU>(src, dst, lo, hi, a.vec != 0);
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    atomicAdd(reinterpret_cast<unsigned long long*>(a.cnt + (size_t)q * a.ncnt),
+                              (unsigned long long)(k1 - k0));          // local completion
+                    red_release_add_u64(a.sig + (size_t)p * a.nsig + q, 1ull);   // strong signal
+                }
+            }
+        }
+    }
+    // ---- receivers: wait on every (p, q) signal; optionally check prefixes
+    const bool dedicated = a.nproducers < gridDim.x;
+    const uint32_t w0 = dedicated ? blockIdx.x - a.nproducers : blockIdx.x;
+    const uint32_t ws = dedicated ? gridDim.x - a.nproducers : gridDim.x;
+    if (dedicated && blockIdx.x < a.nproducers) return;
+    uint32_t parity = 0;
+    for (uint32_t pr = w0; pr < pairs; pr += ws) {
+        const uint32_t p = pr / R, q = pr - p * R;
+        const uint64_t* sp = a.sig + (size_t)p * a.nsig + q;
+        if (!a.mismatch) {
+            if (threadIdx.x == 0) {
+                const uint64_t want = a.nbatches;
+                if (!bounded_spin([&] { return ld_acquire_u64(sp) >= want; }, a.timeout_ns,
+                                  a.status))
+                    report_timeout(a.status, kSitePutSignalRecv, p, q);
+            }
+            continue;
+        }
+        const char* src = a.send + (size_t)q * a.sstride;
+        const char* seg = a.recv + (size_t)p * a.rstride + (size_t)q * a.S;
+        uint64_t seen = 0;
+        while (seen < a.nbatches) {
+            if (threadIdx.x == 0) {
+                uint64_t v = 0;
+                const uint64_t s0 = seen;
+                bool got = bounded_spin([&] { return (v = ld_acquire_u64(sp)) > s0; },
+                                        a.timeout_ns, a.status);
+                if (!got) report_timeout(a.status, kSitePutSignalRecv, p, q);
+                s_v[parity] = got ? min(v, (uint64_t)a.nbatches) : ~0ull;
+            }
+            __syncthreads();
+            const uint64_t v = s_v[parity];
+            parity ^= 1u;
+            if (v == ~0ull) break;
+            // batches [seen, v) must already equal the source
+            const size_t lo = (size_t)seen * a.B * a.chunk;
+            const size_t hi = min((size_t)v * a.B * a.chunk, a.S);
+            uint64_t bad = 0;
+            for (size_t i = lo + threadIdx.x; i < hi; i += kPutThreads)
+                bad += (__ldcg(reinterpret_cast<const unsigned char*>(seg + i)) !=
+                        __ldcg(reinterpret_cast<const unsigned char*>(src + i)));
+            bad = block_sum_u64(bad, s_red);
+            if (threadIdx.x == 0 && bad)
+                atomicAdd(reinterpret_cast<unsigned long long*>(a.mismatch),
+                          (unsigned long long)bad);
+            seen = v;
+        }
+    }
+}
+
+__global__ void k_reset_slots(uint64_t* sig, uint32_t nsig, uint64_t* cnt, uint32_t ncnt, int R) {
+    for (int i = threadIdx.x; i < R * R; i += blockDim.x) {
+        const int p = i / R, q = i - p * R;
+        sig[(size_t)p * nsig + q] = 0;
+    }
+    for (int q = threadIdx.x; q < R; q += blockDim.x) cnt[(size_t)q * ncnt] = 0;
+}
+
+// ----------------------------------------------------------------- single put
+
+struct PutArgs {
+    const char* src;
+    char* dst;
+    size_t bytes;
+    int vec;
+    uint64_t* sig;            // nullable
+    uint64_t* cnt;            // nullable
+    uint32_t* arrive;         // arrival counter of this launch (zero on entry)
+};
+
+__global__ void __launch_bounds__(kPutThreads) k_put(PutArgs a) {
+    // this CTA's share of the bytes, 16-byte aligned
+    const size_t per = ((a.bytes + gridDim.x - 1) / gridDim.x + 15) / 16 * 16;
+    const size_t lo = min((size_t)blockIdx.x * per, a.bytes), hi = min(lo + per, a.bytes);
+    block_copy<kPutThreads, kPutU>(a.src, a.dst, lo, hi, a.vec != 0);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(a.arrive, 1u);
+        if (prev == gridDim.x - 1) {            // last CTA: every byte is in place
+            *a.arrive = 0;
+            __threadfence();
+            if (a.cnt) atomicAdd(reinterpret_cast<unsigned long long*>(a.cnt), 1ull);
+            if (a.sig) red_release_add_u64(a.sig, 1ull);
+        }
+    }
+}
+
+__global__ void k_signal_add(uint64_t* sig, uint64_t value) {
+    __threadfence();
+    red_release_add_u64(sig, value);
+}
+
+__global__ void k_wait_slot(const uint64_t* slot, uint64_t least, int bits, uint64_t timeout_ns,
+                            uint32_t* status, uint32_t site, uint32_t a, uint32_t b) {
+    if (threadIdx.x != 0) return;
+    bool ok = bounded_spin([&] { return rolling_le_dev(least, ld_acquire_u64(slot), bits); },
+                           timeout_ns, status);
+    if (!ok) report_timeout(status, site, a, b);
+}
+
+}  // namespace symar
+
+using namespace symar;
+
+static bool same_group(sym_win_t a, sym_win_t b) {
+    return a && b && a->R == b->R && a->device == b->device;
+}
+
+static sym_status_t launch_put_signal_allgather(sym_win_t send, sym_win_t recv, size_t S,
+                                                size_t chunk, uint32_t B, uint64_t* d_mismatch,
+                                                uint64_t timeout_ns, cudaStream_t st) {
+    const int R = send->R;
+    if (recv->nsignals < (uint32_t)R || send->ncounters < 1) return SYM_ERR_INVALID_ARG;
+    if (chunk == 0) chunk = 64 * 1024;
+    if (B == 0) B = 8;
+    const size_t nchunks = ceil_div(S, chunk);
+    if (nchunks > 0xFFFFFFFFull) return SYM_ERR_INVALID_ARG;
+    PsArgs a{};
+    a.send = send->base;
+    a.recv = recv->base;
+    a.sstride = send->stride;
+    a.rstride = recv->stride;
+    a.R = R;
+    a.S = S;
+    a.chunk = chunk;
+    a.B = B;
+    a.nchunks = (uint32_t)nchunks;
+    a.nbatches = (uint32_t)ceil_div(nchunks, (size_t)B);
+    a.sig = recv->sig;
+    a.nsig = recv->nsignals;
+    a.cnt = send->cnt;
+    a.ncnt = send->ncounters;
+    a.mismatch = d_mismatch;
+    a.status = recv->ctx->status;
+    a.timeout_ns = timeout_ns ? timeout_ns : default_timeout_ns();
+    if (a.timeout_ns > 60000000000ull) a.timeout_ns = 60000000000ull;
+    a.vec = (S % 16 == 0 && chunk % 16 == 0) ? 1 : 0;
+    k_reset_slots<<<1, 256, 0, st>>>(a.sig, a.nsig, a.cnt, a.ncnt, R);
+    count_launch();
+    const int occ = occupancy((const void*)k_put_signal_allgather, kPutThreads, 0);
+    const size_t cap = (size_t)occ * recv->ctx->num_sms;
+    const size_t pairs = (size_t)R * R;
+    size_t waiters = d_mismatch ? std::min(pairs, std::max(cap / 2, (size_t)1)) : 0;
+    size_t producers = std::min(pairs, cap - waiters);
+    if (producers == 0) {
+        producers = 1;
+        waiters = cap > 1 ? 1 : 0;
+    }
+    a.nproducers = (uint32_t)producers;
+    const size_t grid = producers + waiters;
+    void* args[] = {&a};
+    // receivers wait on senders in the same launch -> co-residency required
+    SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_put_signal_allgather, dim3((unsigned)grid),
+                                         dim3(kPutThreads), args, 0, st));
+    count_launch();
+    if (trace_on())
+        fprintf(stderr, "[symar] put_signal_allgather R=%d S=%zu chunk=%zu B=%u grid=%zu+%zu\n", R,
+                S, chunk, B, producers, waiters);
+    return SYM_OK;
+}
+
+extern "C" {
+
+sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym_dtype_t dtype,
+                           sym_algo_t algo, size_t chunk_bytes, uint32_t chunks_per_signal,
+                           sym_stream_t stream) {
+    if (!same_group(send, recv) || send == recv || send->base == recv->base)
+        return SYM_ERR_INVALID_ARG;
+    const size_t es = dtype_size(dtype);
+    if (!es) return SYM_ERR_INVALID_ARG;
+    if (algo != SYM_ALGO_AUTO && algo != SYM_ALGO_COPY && algo != SYM_ALGO_PUT_SIGNAL)
+        return SYM_ERR_INVALID_ARG;
+    const int R = send->R;
+    if (sendcount > send->bytes / es) return SYM_ERR_INVALID_ARG;
+    const size_t S = sendcount * es;
+    if (S > recv->bytes / (size_t)R) return SYM_ERR_INVALID_ARG;
+    if (S == 0) return SYM_OK;
+    DeviceGuard g(recv->device);
+    if (!g.ok) return SYM_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (algo == SYM_ALGO_PUT_SIGNAL) {
+        sym_status_t s = launch_put_signal_allgather(send, recv, S, chunk_bytes, chunks_per_signal,
+                                                     nullptr, 0, st);
+        if (s != SYM_OK) return s;
+        SYM_CUDA(cudaGetLastError());
+        return SYM_OK;
+    }
+    AgArgs a{};
+    a.send = send->base;
+    a.recv = recv->base;
+    a.sstride = send->stride;
+    a.rstride = recv->stride;
+    a.R = R;
+    a.S = S;
+    const int sms = recv->ctx->num_sms;
+    if (S % 16 == 0) {
+        a.nvec = S / 16;
+        a.tiles = (uint32_t)ceil_div(a.nvec, (size_t)kCopyThreads * kCopyU);
+        const size_t items = (size_t)R * a.tiles;
+        const int occ = occupancy((const void*)k_allgather_copy, kCopyThreads, 0);
+        const size_t grid = std::min(items, (size_t)occ * sms);
+        k_allgather_copy<<<(unsigned)grid, kCopyThreads, 0, st>>>(a);
+    } else {
+        const size_t total = (size_t)R * S;
+        const size_t grid = std::min(ceil_div(total, (size_t)256), (size_t)sms * 8);
+        k_allgather_bytes<<<(unsigned)grid, 256, 0, st>>>(a);
+    }
+    count_launch();
+    SYM_CUDA(cudaGetLastError());
+    return SYM_OK;
+}
+
+sym_status_t sym_allgather_put_signal(sym_win_t send, sym_win_t recv, size_t bytes_per_rank,
+                                      size_t chunk_bytes, uint32_t chunks_per_signal,
+                                      uint64_t* d_mismatch, uint64_t timeout_ns,
+                                      sym_stream_t stream) {
+    if (!same_group(send, recv) || send == recv || send->base == recv->base)
+        return SYM_ERR_INVALID_ARG;
+    const int R = send->R;
+    if (bytes_per_rank > send->bytes || bytes_per_rank > recv->bytes / (size_t)R)
+        return SYM_ERR_INVALID_ARG;
+    if (bytes_per_rank == 0) return SYM_OK;
+    DeviceGuard g(recv->device);
+    if (!g.ok) return SYM_ERR_CUDA;
+    sym_status_t s = launch_put_signal_allgather(send, recv, bytes_per_rank, chunk_bytes,
+                                                 chunks_per_signal, d_mismatch, timeout_ns,
+                                                 (cudaStream_t)stream);
+    if (s != SYM_OK) return s;
+    SYM_CUDA(cudaGetLastError());
+    return SYM_OK;
+}
+
+sym_status_t sym_put_signal(sym_win_t src, sym_win_t dst, int src_rank, int peer, size_t dst_off,
+                            size_t src_off, size_t bytes, uint32_t signal_id, uint32_t counter_id,
+                            sym_stream_t stream) {
+    if (!src || !dst || src->device != dst->device) return SYM_ERR_INVALID_ARG;
+    if (src_rank < 0 || src_rank >= src->R || peer < 0 || peer >= dst->R) return SYM_ERR_INVALID_ARG;
+    if (src_off > src->bytes || bytes > src->bytes - src_off) return SYM_ERR_INVALID_ARG;
+    if (dst_off > dst->bytes || bytes > dst->bytes - dst_off) return SYM_ERR_INVALID_ARG;
+    if (signal_id != UINT32_MAX && signal_id >= dst->nsignals) return SYM_ERR_INVALID_ARG;
+    if (counter_id != UINT32_MAX && counter_id >= src->ncounters) return SYM_ERR_INVALID_ARG;
+    const char* s = src->base + (size_t)src_rank * src->stride + src_off;
+    char* d = dst->base + (size_t)peer * dst->stride + dst_off;
+    if (bytes && s < d + bytes && d < s + bytes) return SYM_ERR_INVALID_ARG;   // overlap
+    DeviceGuard g(dst->device);
+    if (!g.ok) return SYM_ERR_CUDA;
+    DevCtx* ctx = dst->ctx;
+    PutArgs a{};
+    a.src = s;
+    a.dst = d;
+    a.bytes = bytes;
+    a.vec = ((((uintptr_t)s | (uintptr_t)d | bytes) & 15u) == 0) ? 1 : 0;
+    a.sig = signal_id != UINT32_MAX ? dst->sig + (size_t)peer * dst->nsignals + signal_id : nullptr;
+    a.cnt = counter_id != UINT32_MAX ? src->cnt + (size_t)src_rank * src->ncounters + counter_id
+                                     : nullptr;
+    a.arrive = ctx->arrive + (ctx->arrive_next++ % kArriveRing);
+    const size_t per_cta = 64 * 1024;
+    const size_t grid = std::max((size_t)1, std::min(ceil_div(bytes, per_cta),
+                                                     (size_t)ctx->num_sms * 4));
+    k_put<<<(unsigned)grid, kPutThreads, 0, (cudaStream_t)stream>>>(a);
+    count_launch();
+    SYM_CUDA(cudaGetLastError());
+    return SYM_OK;
+}
+
+sym_status_t sym_signal(sym_win_t dst, int peer, uint32_t signal_id, uint64_t value,
+                        sym_stream_t stream) {
+    if (!dst || peer < 0 || peer >= dst->R || signal_id >= dst->nsignals) return SYM_ERR_INVALID_ARG;
+    DeviceGuard g(dst->device);
+    k_signal_add<<<1, 1, 0, (cudaStream_t)stream>>>(
+        dst->sig + (size_t)peer * dst->nsignals + signal_id, value);
+    count_launch();
+    SYM_CUDA(cudaGetLastError());
+    return SYM_OK;
+}
+
+static sym_status_t wait_slot(sym_win_t w, const uint64_t* slot, uint64_t least, int bits,
+                              uint64_t timeout_ns, uint32_t site, uint32_t a, uint32_t b,
+                              sym_stream_t stream) {
+    if (timeout_ns == 0) timeout_ns = default_timeout_ns();
+    if (timeout_ns > 60000000000ull) timeout_ns = 60000000000ull;
+    DeviceGuard g(w->device);
+    k_wait_slot<<<1, 32, 0, (cudaStream_t)stream>>>(slot, least, bits, timeout_ns, w->ctx->status,
+                                                    site, a, b);
+    count_launch();
+    SYM_CUDA(cudaGetLastError());
+    return SYM_OK;
+}
+
+sym_status_t sym_signal_wait(sym_win_t w, int rank, uint32_t signal_id, uint64_t least, int bits,
+                             uint64_t timeout_ns, sym_stream_t stream) {
+    if (!w || rank < 0 || rank >= w->R || signal_id >= w->nsignals) return SYM_ERR_INVALID_ARG;
+    if (bits < 1 || bits > 64) return SYM_ERR_INVALID_ARG;
+    return wait_slot(w, w->sig + (size_t)rank * w->nsignals + signal_id, least, bits, timeout_ns,
+                     kSiteSignalWait, (uint32_t)rank, signal_id, stream);
+}
+
+sym_status_t sym_counter_wait(sym_win_t w, int rank, uint32_t counter_id, uint64_t least, int bits,
+                              uint64_t timeout_ns, sym_stream_t stream) {
+    if (!w || rank < 0 || rank >= w->R || counter_id >= w->ncounters) return SYM_ERR_INVALID_ARG;
+    if (bits < 1 || bits > 56) return SYM_ERR_INVALID_ARG;
+    return wait_slot(w, w->cnt + (size_t)rank * w->ncounters + counter_id, least, bits, timeout_ns,
+                     kSiteCounterWait, (uint32_t)rank, counter_id, stream);
+}
+
+static sym_status_t read_slot(sym_win_t w, const uint64_t* slot, int bits, uint64_t* out,
+                              sym_stream_t stream) {
+    DeviceGuard g(w->device);
+    uint64_t v = 0;
+    SYM_CUDA(cudaMemcpyAsync(&v, slot, sizeof v, cudaMemcpyDeviceToHost, (cudaStream_t)stream));
+    SYM_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    *out = bits >= 64 ? v : (v & ((1ull << bits) - 1ull));
+    return SYM_OK;
+}
+
+sym_status_t sym_signal_read(sym_win_t w, int rank, uint32_t signal_id, int bits, uint64_t* out,
+                             sym_stream_t stream) {
+    if (!w || !out || rank < 0 || rank >= w->R || signal_id >= w->nsignals) return SYM_ERR_INVALID_ARG;
+    if (bits < 1 || bits > 64) return SYM_ERR_INVALID_ARG;
+    return read_slot(w, w->sig + (size_t)rank * w->nsignals + signal_id, bits, out, stream);
+}
+
+sym_status_t sym_counter_read(sym_win_t w, int rank, uint32_t counter_id, int bits, uint64_t* out,
+                              sym_stream_t stream) {
+    if (!w || !out || rank < 0 || rank >= w->R || counter_id >= w->ncounters)
+        return SYM_ERR_INVALID_ARG;
+    if (bits < 1 || bits > 56) return SYM_ERR_INVALID_ARG;
+    return read_slot(w, w->cnt + (size_t)rank * w->ncounters + counter_id, bits, out, stream);
+}
+
+sym_status_t sym_signal_reset(sym_win_t w, int rank, uint32_t signal_id, sym_stream_t stream) {
+    if (!w || rank < 0 || rank >= w->R || signal_id >= w->nsignals) return SYM_ERR_INVALID_ARG;
+    DeviceGuard g(w->device);
+    SYM_CUDA(cudaMemsetAsync(w->sig + (size_t)rank * w->nsignals + signal_id, 0, sizeof(uint64_t),
+                             (cudaStream_t)stream));
+    return SYM_OK;
+}
+
+sym_status_t sym_counter_reset(sym_win_t w, int rank, uint32_t counter_id, sym_stream_t stream) {
+    if (!w || rank < 0 || rank >= w->R || counter_id >= w->ncounters) return SYM_ERR_INVALID_ARG;
+    DeviceGuard g(w->device);
+    SYM_CUDA(cudaMemsetAsync(w->cnt + (size_t)rank * w->ncounters + counter_id, 0, sizeof(uint64_t),
+                             (cudaStream_t)stream));
+    return SYM_OK;
+}
+
+}  // extern "C"

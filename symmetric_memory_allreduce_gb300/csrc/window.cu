@@ -1,0 +1,306 @@
+// Symmetric windows: allocation, registration, addressing, host copies,
+// per-device status, and the library's host-side bookkeeping.
+//
+// [SYMEX] "NCCL symmetric memory windows" guide: ncclMemAlloc and
+// ncclCommWindowRegister(NCCL_WIN_COLL_SYMMETRIC) give every rank a buffer of
+// the same size and layout, registration requires 4096-byte alignment, and
+// windows are deregistered before their memory is freed.  Here all R ranks
+// live in one allocation at base + r*stride ([LSA] "base plus offset"), so a
+// peer address is pure integer arithmetic and every kernel can reach every
+// rank with ordinary loads and stores.
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+
+#include "symar_internal.cuh"
+
+namespace symar {
+
+static thread_local char g_last_error[256] = "";
+static std::atomic<uint64_t> g_launches{0};
+
+sym_status_t cuda_fail(cudaError_t e, const char* what) {
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", what, cudaGetErrorString(e),
+             cudaGetErrorName(e));
+    if (trace_on()) fprintf(stderr, "[symar] CUDA error %s\n", g_last_error);
+    return e == cudaErrorMemoryAllocation ? SYM_ERR_OOM : SYM_ERR_CUDA;
+}
+
+DeviceGuard::DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+        prev = -1;
+        ok = false;
+        return;
+    }
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+}
+
+DeviceGuard::~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+}
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+static uint64_t env_u64(const char* name, uint64_t dflt) {
+    const char* s = getenv(name);
+    if (!s || !*s) return dflt;
+    char* end = nullptr;
+    unsigned long long v = strtoull(s, &end, 0);
+    return (end && *end == 0) ? (uint64_t)v : dflt;
+}
+
+bool trace_on() {
+    static const bool on = env_u64("SYM_TRACE", 0) != 0;
+    return on;
+}
+
+uint64_t default_timeout_ns() {
+    // bounded: at most 60 s whatever the environment says
+    static const uint64_t t = [] {
+        uint64_t v = env_u64("SYM_TIMEOUT_NS", 2000000000ull);
+        if (v == 0) v = 2000000000ull;
+        return v > 60000000000ull ? 60000000000ull : v;
+    }();
+    return t;
+}
+
+size_t oneshot_max_bytes() {
+    static const size_t v = (size_t)env_u64("SYM_ONESHOT_MAX_BYTES", 16384);
+    return v;
+}
+
+size_t dtype_size(sym_dtype_t t) {
+    switch (t) {
+        case SYM_F32: return 4;
+        case SYM_BF16: return 2;
+        case SYM_F16: return 2;
+    }
+    return 0;
+}
+
+int occupancy(const void* kernel, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(dev, kernel);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess)
+        n = 1;
+    if (n < 1) n = 1;
+    cache[key] = n;
+    return n;
+}
+
+DevCtx* dev_ctx(int device) {
+    static std::mutex mu;
+    static std::map<int, DevCtx*> ctxs;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = ctxs.find(device);
+    if (it != ctxs.end()) return it->second;
+    DeviceGuard g(device);
+    if (!g.ok) return nullptr;
+    DevCtx* c = new DevCtx();
+    c->device = device;
+    if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        c->num_sms = 1;
+    const size_t words = 4 + kArriveRing;
+    uint32_t* mem = nullptr;
+    if (cudaMalloc(&mem, words * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(mem, 0, words * sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        delete c;
+        return nullptr;
+    }
+    c->status = mem;
+    c->arrive = mem + 4;
+    ctxs[device] = c;
+    return c;
+}
+
+}  // namespace symar
+
+using namespace symar;
+
+// Slot arrays and flags for a window: one allocation, zeroed.
+static sym_status_t alloc_aux(sym_window* w) {
+    // pull two-shot: one flag per (rank-slot, tile); a tile is 16 KiB of a chunk
+    const size_t tile_bytes = 16384;
+    size_t chunk_bytes = ceil_div(ceil_div(w->bytes, (size_t)kVecBytes), (size_t)w->R) * kVecBytes;
+    w->flag_tiles = ceil_div(chunk_bytes, tile_bytes) + 1;
+    size_t sig_b = sizeof(uint64_t) * (size_t)w->R * w->nsignals;
+    size_t cnt_b = sizeof(uint64_t) * (size_t)w->R * w->ncounters;
+    size_t flg_b = sizeof(uint32_t) * (size_t)w->R * w->flag_tiles;
+    size_t total = sig_b + cnt_b + flg_b;
+    char* p = nullptr;
+    SYM_CUDA(cudaMalloc(&p, total));
+    cudaError_t e = cudaMemset(p, 0, total);
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        return cuda_fail(e, "cudaMemset(window slots)");
+    }
+    w->aux = p;
+    w->sig = (uint64_t*)p;
+    w->cnt = (uint64_t*)(p + sig_b);
+    w->flags = (uint32_t*)(p + sig_b + cnt_b);
+    w->epoch = 0;
+    return SYM_OK;
+}
+
+static sym_status_t make_window(void* base, bool owns, int R, size_t bytes, size_t stride,
+                                uint32_t nsig, uint32_t ncnt, sym_win_t* out) {
+    int dev = 0;
+    SYM_CUDA(cudaGetDevice(&dev));
+    DevCtx* ctx = dev_ctx(dev);
+    if (!ctx) return SYM_ERR_CUDA;
+    sym_window* w = new sym_window();
+    w->device = dev;
+    w->R = R;
+    w->bytes = bytes;
+    w->stride = stride;
+    w->owns_base = owns;
+    w->nsignals = nsig;
+    w->ncounters = ncnt;
+    w->ctx = ctx;
+    w->aux = nullptr;
+    if (owns) {
+        char* p = nullptr;
+        cudaError_t e = cudaMalloc(&p, stride * (size_t)R);
+        if (e != cudaSuccess) {
+            delete w;
+            return cuda_fail(e, "cudaMalloc(window)");
+        }
+        w->base = p;
+    } else {
+        w->base = (char*)base;
+    }
+    sym_status_t s = alloc_aux(w);
+    if (s != SYM_OK) {
+        if (owns) cudaFree(w->base);
+        delete w;
+        return s;
+    }
+    *out = w;
+    return SYM_OK;
+}
+
+extern "C" {
+
+sym_status_t sym_window_alloc(int R, size_t bytes_per_rank, uint32_t nsignals, uint32_t ncounters,
+                              sym_win_t* out) {
+    if (!out) return SYM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (R < 1 || R > kMaxRanks || bytes_per_rank == 0) return SYM_ERR_INVALID_ARG;
+    if (nsignals > (1u << 20) || ncounters > (1u << 20)) return SYM_ERR_INVALID_ARG;
+    if (bytes_per_rank > ((size_t)1 << 40)) return SYM_ERR_INVALID_ARG;
+    size_t stride = ceil_div(bytes_per_rank, kWindowAlign) * kWindowAlign;
+    return make_window(nullptr, true, R, bytes_per_rank, stride, nsignals, ncounters, out);
+}
+
+sym_status_t sym_window_register(void* base, int R, size_t bytes_per_rank, size_t stride,
+                                 uint32_t nsignals, uint32_t ncounters, sym_win_t* out) {
+    if (!out) return SYM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!base || R < 1 || R > kMaxRanks || bytes_per_rank == 0) return SYM_ERR_INVALID_ARG;
+    if (((uintptr_t)base & 255u) != 0 || stride % kWindowAlign != 0 || stride < bytes_per_rank)
+        return SYM_ERR_INVALID_ARG;
+    if (nsignals > (1u << 20) || ncounters > (1u << 20)) return SYM_ERR_INVALID_ARG;
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, base);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return SYM_ERR_INVALID_ARG;
+    int dev = 0;
+    SYM_CUDA(cudaGetDevice(&dev));
+    if (attr.device != dev) return SYM_ERR_INVALID_ARG;
+    return make_window(base, false, R, bytes_per_rank, stride, nsignals, ncounters, out);
+}
+
+sym_status_t sym_window_free(sym_win_t w) {
+    if (!w) return SYM_OK;
+    DeviceGuard g(w->device);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (w->aux) cudaFree(w->aux);
+    if (w->owns_base && w->base) cudaFree(w->base);
+    delete w;
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize(window_free)");
+    return SYM_OK;
+}
+
+sym_status_t sym_window_rank_ptr(sym_win_t w, int rank, void** dptr) {
+    if (!w || !dptr || rank < 0 || rank >= w->R) return SYM_ERR_INVALID_ARG;
+    *dptr = w->base + (size_t)rank * w->stride;
+    return SYM_OK;
+}
+
+size_t sym_window_stride(sym_win_t w) { return w ? w->stride : 0; }
+size_t sym_window_bytes(sym_win_t w) { return w ? w->bytes : 0; }
+int sym_window_nranks(sym_win_t w) { return w ? w->R : 0; }
+int sym_window_device(sym_win_t w) { return w ? w->device : -1; }
+
+sym_status_t sym_window_write(sym_win_t w, int rank, size_t off, const void* src, size_t bytes,
+                              sym_stream_t stream) {
+    if (!w || rank < 0 || rank >= w->R || (!src && bytes)) return SYM_ERR_INVALID_ARG;
+    if (off > w->bytes || bytes > w->bytes - off) return SYM_ERR_INVALID_ARG;
+    if (bytes == 0) return SYM_OK;
+    DeviceGuard g(w->device);
+    SYM_CUDA(cudaMemcpyAsync(w->base + (size_t)rank * w->stride + off, src, bytes, cudaMemcpyDefault,
+                             (cudaStream_t)stream));
+    return SYM_OK;
+}
+
+sym_status_t sym_window_read(sym_win_t w, int rank, size_t off, void* dst, size_t bytes,
+                             sym_stream_t stream) {
+    if (!w || rank < 0 || rank >= w->R || (!dst && bytes)) return SYM_ERR_INVALID_ARG;
+    if (off > w->bytes || bytes > w->bytes - off) return SYM_ERR_INVALID_ARG;
+    if (bytes == 0) return SYM_OK;
+    DeviceGuard g(w->device);
+    SYM_CUDA(cudaMemcpyAsync(dst, w->base + (size_t)rank * w->stride + off, bytes, cudaMemcpyDefault,
+                             (cudaStream_t)stream));
+    return SYM_OK;
+}
+
+sym_status_t sym_stream_status(sym_stream_t stream) {
+    int dev = 0;
+    SYM_CUDA(cudaGetDevice(&dev));
+    SYM_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    SYM_CUDA(cudaGetLastError());
+    DevCtx* c = dev_ctx(dev);
+    if (!c) return SYM_ERR_CUDA;
+    uint32_t st[4] = {0, 0, 0, 0};
+    SYM_CUDA(cudaMemcpy(st, c->status, sizeof st, cudaMemcpyDeviceToHost));
+    if (st[0] == 0) return SYM_OK;
+    snprintf(g_last_error, sizeof g_last_error, "device status 0x%x at site %u (%u, %u)", st[0],
+             st[1], st[2], st[3]);
+    SYM_CUDA(cudaMemset(c->status, 0, sizeof st));
+    if (st[0] & kStatusTimeout) return SYM_ERR_TIMEOUT;
+    return SYM_ERR_DEVICE_STATUS;
+}
+
+const char* sym_status_string(sym_status_t s) {
+    switch (s) {
+        case SYM_OK: return "SYM_OK";
+        case SYM_ERR_INVALID_ARG: return "SYM_ERR_INVALID_ARG";
+        case SYM_ERR_OOM: return "SYM_ERR_OOM";
+        case SYM_ERR_CUDA: return "SYM_ERR_CUDA";
+        case SYM_ERR_TIMEOUT: return "SYM_ERR_TIMEOUT";
+        case SYM_ERR_UNSUPPORTED: return "SYM_ERR_UNSUPPORTED";
+        case SYM_ERR_DEVICE_STATUS: return "SYM_ERR_DEVICE_STATUS";
+    }
+    return "SYM_ERR_UNKNOWN";
+}
+
+const char* sym_last_error(void) { return g_last_error; }
+
+uint64_t sym_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int sym_abi_version(void) { return SYMAR_ABI_VERSION; }
+
+}  // extern "C"

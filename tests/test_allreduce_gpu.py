@@ -1,0 +1,289 @@
+"""AllReduce parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+fp32: bit-exact (same rank order, IEEE adds).  bf16: within 1 ulp of the
+oracle's fp32-accumulated, once-rounded result (expected bit-exact as well;
+the exact-match count is asserted separately).
+"""
+import numpy as np
+import pytest
+
+from _gpu_util import bf16_ulp_distance, download, sync, upload
+
+pytestmark = pytest.mark.gpu
+
+ALGOS = ["oneshot", "twoshot", "twoshot_pull", "twoshot_split"]
+
+
+def _run(sm, x, dtype, algo, in_place=False, nsig=0):
+    """x: (R, n) float32 or uint16 (bf16 bits). Returns (R, n) results of every rank."""
+    R, n = x.shape
+    es = x.itemsize
+    send = sm.Window(R, max(n * es, 16))
+    recv = send if in_place else sm.Window(R, max(n * es, 16))
+    try:
+        upload(send, x)
+        sm.sym_allreduce(send, recv, n, dtype, "sum", algo)
+        assert sm.sym_stream_status() == sm.SYM_OK
+        return download(recv, n * es, x.dtype)
+    finally:
+        send.free()
+        if not in_place:
+            recv.free()
+
+
+def _check_f32(y, want):
+    assert np.array_equal(y.view(np.uint32), np.broadcast_to(want.view(np.uint32), y.shape))
+
+
+def _check_bf16(y, want):
+    d = bf16_ulp_distance(y, np.broadcast_to(want, y.shape))
+    assert d.max(initial=0) <= 1
+    assert np.array_equal(y, np.broadcast_to(want, y.shape))     # same order, one rounding
+
+
+def test_worked_example_rankfill(symar, oracle):
+    """4 ranks of 1,048,576 floats filled with their rank: every element 6.0."""
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    x = wl.config_inputs(1, dist="rankfill")
+    for algo in ALGOS:
+        y = _run(symar, x, "f32", algo)
+        assert np.all(np.abs(y - 6.0) <= 0.001)
+        assert np.all(y == np.float32(6.0))
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_config1_normal(symar, oracle, algo):
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    x = wl.config_inputs(1, dist="normal")
+    _check_f32(_run(symar, x, "f32", algo), oracle.allreduce_sum_f32(x))
+
+
+# ragged sizes that span several tiles: fp32 tile = 2048 (two-shot/one-shot)
+# or 4096 (pull) elements per slot chunk; tails of 1..V-1 elements
+SIZES = [1, 3, 4, 5, 7, 8, 9, 63, 1000, 4097, 65_539, 100_003, 262_147]
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("algo", ALGOS)
+def test_ragged_f32(symar, oracle, R, algo):
+    rng = np.random.default_rng(100 + R)
+    for n in SIZES:
+        x = rng.standard_normal((R, n)).astype(np.float32)
+        _check_f32(_run(symar, x, "f32", algo), oracle.allreduce_sum_f32(x))
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("algo", ALGOS)
+def test_ragged_bf16(symar, oracle, R, algo):
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    rng = np.random.default_rng(200 + R)
+    for n in SIZES:
+        x = wl.to_bf16_bits(rng.uniform(-1, 1, size=(R, n)).astype(np.float32))
+        _check_bf16(_run(symar, x, "bf16", algo), oracle.allreduce_sum_bf16(x))
+
+
+@pytest.mark.parametrize("algo", ["twoshot", "twoshot_pull", "twoshot_split"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_in_place(symar, oracle, algo, dtype):
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    rng = np.random.default_rng(7)
+    for R, n in [(8, 100_003), (3, 4097), (16, 65_539)]:
+        xf = rng.standard_normal((R, n)).astype(np.float32)
+        if dtype == "f32":
+            _check_f32(_run(symar, xf, "f32", algo, in_place=True), oracle.allreduce_sum_f32(xf))
+        else:
+            xb = wl.to_bf16_bits(xf)
+            _check_bf16(_run(symar, xb, "bf16", algo, in_place=True), oracle.allreduce_sum_bf16(xb))
+
+
+def test_in_place_oneshot_rejected(symar):
+    w = symar.Window(4, 4096)
+    try:
+        with pytest.raises(symar.SymError) as e:
+            symar.sym_allreduce(w, w, 16, "f32", "sum", "oneshot")
+        assert e.value.status == symar.SYM_ERR_UNSUPPORTED
+    finally:
+        w.free()
+
+
+def test_order_sensitive_values(symar, oracle):
+    """Values whose sum depends on the order: only rank order 0..R-1 matches."""
+    n = 5000
+    x = np.empty((4, n), np.float32)
+    x[0], x[1], x[2], x[3] = 1e8, 1.0, -1e8, 1.0        # forward 1.0, tree 0.0
+    want = oracle.allreduce_sum_f32(x)
+    assert np.all(want == 1.0)
+    for algo in ALGOS:
+        _check_f32(_run(symar, x, "f32", algo), want)
+
+
+def test_special_values(symar, oracle):
+    """Subnormals are not flushed; -0.0, inf and NaN propagate like the oracle."""
+    tiny = np.float32(1e-45)
+    base = np.array([tiny, -0.0, 1e-40, np.inf, 3.0, -2.5, 1e38, 1e38], np.float32)
+    x = np.stack([base, base, np.roll(base, 1)]).astype(np.float32)
+    x = np.tile(x, (1, 1000))
+    want = oracle.allreduce_sum_f32(x)
+    nan = np.isnan(want)
+    for algo in ALGOS:
+        y = _run(symar, x, "f32", algo)
+        assert np.all(np.isnan(y[:, nan]))
+        assert np.array_equal(y[:, ~nan].view(np.uint32),
+                              np.broadcast_to(want[~nan].view(np.uint32), y[:, ~nan].shape))
+
+
+def test_zero_count_and_validation(symar):
+    a, b = symar.Window(4, 4096), symar.Window(8, 4096)
+    try:
+        n0 = symar.sym_launch_count()
+        symar.sym_allreduce(a, a, 0, "f32", "sum", "twoshot")            # no-op
+        assert symar.sym_launch_count() == n0
+        for bad in [lambda: symar.sym_allreduce(a, b, 16),               # different R
+                    lambda: symar.sym_allreduce(a, a, 1025),             # too many elements
+                    lambda: symar.sym_allreduce(a, a, 16, "f32", "sum", 99)]:
+            with pytest.raises(symar.SymError) as e:
+                bad()
+            assert e.value.status == symar.SYM_ERR_INVALID_ARG
+        with pytest.raises(symar.SymError) as e:
+            symar.sym_allreduce(a, a, 16, "f32", "max", "twoshot")
+        assert e.value.status == symar.SYM_ERR_UNSUPPORTED
+    finally:
+        a.free()
+        b.free()
+
+
+def test_repeat_calls_reuse_windows(symar, oracle):
+    """Epoch-tagged flags: repeated pull calls on the same windows need no reset."""
+    rng = np.random.default_rng(3)
+    R, n = 8, 300_001
+    send, recv = symar.Window(R, n * 4), symar.Window(R, n * 4)
+    try:
+        for it in range(5):
+            x = rng.standard_normal((R, n)).astype(np.float32)
+            upload(send, x)
+            symar.sym_allreduce(send, recv, n, "f32", "sum", "twoshot_pull")
+            assert symar.sym_stream_status() == symar.SYM_OK
+            _check_f32(download(recv, n * 4, np.float32), oracle.allreduce_sum_f32(x))
+    finally:
+        send.free()
+        recv.free()
+
+
+def test_registered_torch_memory(symar, oracle):
+    """sym_window_register over a torch allocation (caller-owned memory)."""
+    import torch
+
+    R, n = 4, 70_000
+    stride = ((n * 4 + 4095) // 4096) * 4096
+    buf_s = torch.empty(R * stride, dtype=torch.uint8, device="cuda")
+    buf_r = torch.empty(R * stride, dtype=torch.uint8, device="cuda")
+    send = symar.Window(R, n * 4, base=buf_s.data_ptr(), stride=stride, keepalive=buf_s)
+    recv = symar.Window(R, n * 4, base=buf_r.data_ptr(), stride=stride, keepalive=buf_r)
+    try:
+        x = np.random.default_rng(5).standard_normal((R, n)).astype(np.float32)
+        upload(send, x)
+        symar.sym_allreduce(send, recv, n, "f32", "sum", "twoshot")
+        sync()
+        y = buf_r.view(R, stride)[:, : n * 4].contiguous().view(torch.float32).cpu().numpy()
+        _check_f32(y, oracle.allreduce_sum_f32(x))
+        # the window's own tensor view sees the same memory
+        t = recv.tensor(torch.float32)
+        assert torch.equal(t[:, :n], torch.from_numpy(y).cuda())
+    finally:
+        send.free()
+        recv.free()
+
+
+# ---------------------------------------------------------------- full-size configs
+
+def _full(symar, oracle, x, dtype, algos):
+    R, n = x.shape
+    es = x.itemsize
+    send, recv = symar.Window(R, n * es), symar.Window(R, n * es)
+    try:
+        upload(send, x)
+        if dtype == "f32":
+            want, _ = oracle.allreduce_sum_mt(x, 16)
+        else:
+            want, _ = oracle.allreduce_sum_mt(x, 16)
+        for algo in algos:
+            symar.sym_allreduce(send, recv, n, dtype, "sum", algo)
+            assert symar.sym_stream_status() == symar.SYM_OK
+            for r in range(R):
+                y = download(recv, n * es, x.dtype, ranks=[r])[0]
+                if dtype == "f32":
+                    assert np.array_equal(y.view(np.uint32), want.view(np.uint32)), (algo, r)
+                else:
+                    assert bf16_ulp_distance(y, want).max() <= 1, (algo, r)
+                    assert np.array_equal(y, want), (algo, r)
+            recv.tensor().zero_()
+            sync()
+    finally:
+        send.free()
+        recv.free()
+
+
+def test_config2_full(symar, oracle):
+    """R=8 x 16,777,216 fp32 N(0,1): one-shot and two-shot, every rank bit-exact."""
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    _full(symar, oracle, wl.config_inputs(2), "f32", ALGOS)
+
+
+def test_config3_full_f32(symar, oracle):
+    """R=8 x 67,108,864 fp32 U(-1,1) (256 MiB per rank), two-shot forms."""
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    _full(symar, oracle, wl.config_inputs(3), "f32", ["twoshot", "twoshot_pull", "auto"])
+
+
+def test_config3_full_bf16(symar, oracle):
+    """The same draws rounded to bf16 (128 MiB per rank), fp32 accumulation."""
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    xb = wl.to_bf16_bits(wl.config_inputs(3))
+    _full(symar, oracle, xb, "bf16", ["twoshot", "twoshot_pull"])
+
+
+@pytest.mark.parametrize("nbytes", [1024 * 4 ** k for k in range(10)])
+def test_config4_sweep(symar, oracle, nbytes):
+    """R=8, 1 KiB .. 256 MiB per rank, fp32 N(0,1), every algorithm and AUTO."""
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    x = wl.config_inputs(4, n=nbytes // 4)
+    _full(symar, oracle, x, "f32", ALGOS + ["auto"])
+
+
+def test_config4_sweep_1gib_sampled(symar, oracle):
+    """The 1 GiB-per-rank point: sampled outputs against the oracle (computed one
+    column at a time), plus every rank's output identical on the device."""
+    import torch
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    R, n = 8, (1 << 30) // 4
+    x = wl.config_inputs(4, n=n)
+    send, recv = symar.Window(R, n * 4), symar.Window(R, n * 4)
+    try:
+        upload(send, x)
+        idx = np.sort(np.random.default_rng(1).choice(n, size=1 << 16, replace=False))
+        idx = np.concatenate([idx, [0, n - 1]])
+        want = oracle.allreduce_sum_f32(np.ascontiguousarray(x[:, idx]))
+        del x
+        for algo in ["oneshot", "twoshot", "twoshot_pull"]:
+            symar.sym_allreduce(send, recv, n, "f32", "sum", algo)
+            assert symar.sym_stream_status() == symar.SYM_OK
+            t = recv.tensor(torch.float32)[:, :n]
+            for r in range(1, R):
+                assert torch.equal(t[0], t[r]), (algo, r)
+            got = t[0][torch.from_numpy(idx).cuda()].cpu().numpy()
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), algo
+            del t
+            recv.tensor().zero_()
+            sync()
+    finally:
+        send.free()
+        recv.free()
