@@ -38,7 +38,8 @@ METRIC = "AllReduce algbw GB/s and HBM GB/s (% of peak) at R=8, 256 MB/rank fp32
 R_DEFAULT, N_DEFAULT = 8, 1 << 26
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "twoshot_st_f32_R8_traffic.json")
-KERNEL_SRC = os.path.join(ROOT, "symmetric_memory_allreduce_gb300", "csrc", "allreduce.cu")
+KERNEL_SRC = [os.path.join(ROOT, "symmetric_memory_allreduce_gb300", "csrc", f)
+              for f in ("allreduce_kernels.cuh", "allreduce_f32.cu", "symar_internal.cuh")]
 
 
 # ----------------------------------------------------------------- pure helpers (CPU-testable)
@@ -66,8 +67,11 @@ def measured_peak() -> tuple[float, str]:
 
 
 def kernel_source_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for p in KERNEL_SRC:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(R: int, S: int) -> float | None:
@@ -409,6 +413,56 @@ def run_ours(args) -> int:
     return 0
 
 
+def run_sweep(args) -> int:
+    """Message-size sweep (R=8, 1 KiB .. 1 GiB per rank, fp32 N(0,1)): median kernel time of
+    every algorithm per size, one JSON object per (size, algo) on stdout."""
+    import torch
+
+    import symmetric_memory_allreduce_gb300 as sm
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    torch.cuda.set_device(0)
+    sm.load()
+    stream = torch.cuda.current_stream()
+    R = args.ranks
+    peak, _ = measured_peak()
+    sizes = [s for s in wl.SWEEP_BYTES if s <= args.sweep_max]
+    algos = ["oneshot", "twoshot", "twoshot_pull", "twoshot_split"]
+    for nbytes in sizes:
+        n = nbytes // 4
+        x = wl.normal_f32(4, R, n)
+        send, recv = sm.Window(R, nbytes), sm.Window(R, nbytes)
+        for r in range(R):
+            send.write(r, x[r])
+        stream.synchronize()
+        for algo in algos:
+            iters = max(5, min(2000, int(2e9 / max(nbytes * 2 * R, 1))))
+            for _ in range(5):
+                sm.sym_allreduce(send, recv, n, "f32", "sum", algo)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(iters)]
+            torch.cuda.synchronize()
+            for s, e in ev:
+                s.record(stream)
+                sm.sym_allreduce(send, recv, n, "f32", "sum", algo)
+                e.record(stream)
+            torch.cuda.synchronize()
+            assert sm.sym_stream_status() == sm.SYM_OK
+            ts = [s.elapsed_time(e) for s, e in ev]
+            med = statistics.median(ts)
+            comp = algo_bytes(algo, R, nbytes)["compulsory"]
+            print(json.dumps({"bytes_per_rank": nbytes, "algo": algo, "iters": iters,
+                              "us_median": med * 1e3, "us_p10": percentile(ts, 0.1) * 1e3,
+                              "us_p90": percentile(ts, 0.9) * 1e3,
+                              "algbw_gbs": nbytes / (med * 1e-3) / 1e9,
+                              "hbm_gbs": comp / (med * 1e-3) / 1e9,
+                              "hbm_frac": comp / (med * 1e-3) / 1e9 / peak,
+                              "auto": sm.sym_allreduce_algo(send, n, "f32")}), flush=True)
+        send.free()
+        recv.free()
+    return 0
+
+
 def parse(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,6 +477,9 @@ def parse(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="message-size sweep of every algorithm instead of the contract line")
+    ap.add_argument("--sweep-max", type=int, default=1 << 30)
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)          # at least three untimed warm-up steps
     return a
@@ -432,6 +489,8 @@ def main(argv=None) -> int:
     args = parse(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

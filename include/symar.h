@@ -182,6 +182,21 @@ sym_status_t sym_allgather_put_signal(sym_win_t send, sym_win_t recv, size_t byt
                                       uint64_t* d_mismatch, uint64_t timeout_ns,
                                       sym_stream_t stream);
 
+/* AlltoAll: recv_p[q*B + i] = send_q[p*B + i] for all ranks p, q and bytes
+ * i < B = count*sizeof(dtype); both windows hold R segments of B bytes per
+ * rank.  [GIN] pure-GIN AlltoAll example: every rank puts `count` elements
+ * to every rank (itself included) at my_rank*count of the receiver's buffer,
+ * each put incrementing one signal; the receiver waits for nRanks
+ * increments.  algo COPY (or AUTO): one launch of plain segment copies.
+ * algo PUT_SIGNAL: the same copies, each followed by a release increment of
+ * signal slot 0 of the receiving rank (reset to 0 first, stream-ordered), and
+ * receivers in the same launch wait (bounded by timeout_ns, 0 = default)
+ * until it reaches R; requires recv nsignals >= 1.  send != recv.
+ * Errors: INVALID_ARG, CUDA; a wait that runs out -> SYM_ERR_TIMEOUT from
+ * sym_stream_status(). */
+sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtype_t dtype,
+                          sym_algo_t algo, uint64_t timeout_ns, sym_stream_t stream);
+
 /* ---------------------------------------------------------------- one-sided */
 
 /* put: copy `bytes` from rank src_rank's part of `src` at src_off to rank

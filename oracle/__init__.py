@@ -154,6 +154,22 @@ def allgather(x: np.ndarray) -> np.ndarray:
     return y
 
 
+def alltoall(x: np.ndarray) -> np.ndarray:
+    """x: (R, R*B) uint8 -> (R, R*B) uint8 with recv[p][q*B:(q+1)*B] = send[q][p*B:(p+1)*B]."""
+    x = _rows(x, np.uint8)
+    R, RB = x.shape
+    if RB % R:
+        raise ValueError("each row must hold R equal segments")
+    y = np.empty_like(x)
+    lib = _load()
+    lib.oracle_alltoall.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t,
+                                    ctypes.c_void_p, ctypes.c_size_t]
+    lib.oracle_alltoall.restype = None
+    if x.size:
+        lib.oracle_alltoall(R, RB // R, _ptr(x), RB, _ptr(y), RB)
+    return y
+
+
 def put_signal_allgather(x: np.ndarray, chunk: int, batch: int):
     """Sequential put+signal model. x: (R, S) uint8.
 
@@ -186,3 +202,58 @@ def rolling_le(a: int, b: int, bits: int = 64) -> bool:
 
 def read_bits(v: int, bits: int) -> int:
     return int(_load().oracle_read_bits(v & (2**64 - 1), bits))
+
+
+# ---------------------------------------------------------------- fp16 and reduction operators
+
+_DT = {"f32": 0, "bf16": 1, "f16": 2}
+_OP = {"sum": 0, "max": 1, "min": 2}
+
+
+def _load_ext():
+    lib = _load()
+    if not getattr(lib, "_ext_ready", False):
+        P, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        lib.oracle_f32_to_f16_rne.argtypes = [ctypes.c_float]
+        lib.oracle_f32_to_f16_rne.restype = ctypes.c_uint16
+        lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_f32.restype = ctypes.c_float
+        lib.oracle_f32_to_f16_array.argtypes = [sz, P, P]
+        lib.oracle_f32_to_f16_array.restype = None
+        lib.oracle_apply_op.argtypes = [i32, ctypes.c_float, ctypes.c_float]
+        lib.oracle_apply_op.restype = ctypes.c_float
+        lib.oracle_allreduce.argtypes = [i32, i32, i32, sz, P, sz, P]
+        lib.oracle_allreduce.restype = None
+        lib._ext_ready = True
+    return lib
+
+
+def f32_to_f16(x: np.ndarray) -> np.ndarray:
+    """float32 -> uint16 binary16 patterns, round to nearest even (NaN -> 0x7E00)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    y = np.empty(x.size, np.uint16)
+    if x.size:
+        _load_ext().oracle_f32_to_f16_array(x.size, _ptr(x), _ptr(y))
+    return y
+
+
+def f16_to_f32_scalar(h: int) -> float:
+    return float(_load_ext().oracle_f16_to_f32(h))
+
+
+def apply_op(op: str, a: float, b: float) -> float:
+    return float(_load_ext().oracle_apply_op(_OP[op], a, b))
+
+
+def allreduce(x: np.ndarray, dtype: str = "f32", op: str = "sum") -> np.ndarray:
+    """x: (R, N) float32 (f32) or uint16 bit patterns (bf16, f16) -> (N,) same type.
+
+    Widen exactly, fold in rank order 0..R-1 in fp32 with `op`, narrow once.
+    """
+    want = np.float32 if dtype == "f32" else np.uint16
+    x = _rows(x, want)
+    R, n = x.shape
+    y = np.empty(n, want)
+    if n:
+        _load_ext().oracle_allreduce(_DT[dtype], _OP[op], R, n, _ptr(x), n, _ptr(y))
+    return y

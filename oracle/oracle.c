@@ -110,6 +110,124 @@ void oracle_allreduce_sum_bf16(int R, size_t n, const uint16_t* x, size_t ldx, u
 }
 
 /* ------------------------------------------------------------------------ */
+/* fp16 (IEEE binary16) <-> fp32.                                           */
+/* Widening is exact.  Narrowing rounds to nearest, ties to even, with      */
+/* gradual underflow: below 2^-14 the result is a multiple of 2^-24; values */
+/* of magnitude >= 65520 (half-way between the largest half, 65504, and     */
+/* 2^16) round to Inf; every NaN becomes the quiet NaN 0x7E00.              */
+/* Pins: numpy's float32->float16 conversion on stratified patterns; exact  */
+/* rational nearest-neighbour brute force; hand cases.                      */
+/* ------------------------------------------------------------------------ */
+float oracle_f16_to_f32(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+    uint32_t e = (h >> 10) & 0x1Fu, m = h & 0x3FFu, u;
+    if (e == 0x1Fu) {
+        u = sign | 0x7F800000u | (m << 13);              /* Inf / NaN */
+    } else if (e != 0) {
+        u = sign | ((e + 112u) << 23) | (m << 13);       /* 112 = 127 - 15 */
+    } else if (m == 0) {
+        u = sign;                                         /* +-0 */
+    } else {                                              /* subnormal: m * 2^-24 */
+        int k = 0;
+        while ((m & 0x400u) == 0) { m <<= 1; ++k; }
+        u = sign | ((uint32_t)(113 - k) << 23) | ((m & 0x3FFu) << 13);
+    }
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+uint16_t oracle_f32_to_f16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t a = u & 0x7FFFFFFFu;
+    if (a > 0x7F800000u) return (uint16_t)0x7E00u;       /* NaN */
+    if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);   /* >= 65520 or Inf */
+    int e = (int)(a >> 23) - 127;
+    uint32_t m = a & 0x7FFFFFu;
+    if (e >= -14) {                                       /* normal half */
+        uint32_t h = ((uint32_t)(e + 15) << 10) | (m >> 13);
+        uint32_t rem = m & 0x1FFFu;
+        if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h += 1u;
+        return (uint16_t)(sign | h);
+    }
+    /* below the normal range: count units of 2^-24, round to nearest even */
+    if ((a >> 23) == 0) return sign;                      /* fp32 subnormal: < 2^-126 */
+    uint64_t M = (uint64_t)(m | 0x800000u);               /* value = M * 2^(e-23) */
+    int s = -(e + 1);                                     /* units of 2^-24: M >> s */
+    if (s >= 40) return sign;
+    uint64_t q = M >> s, rem = M & (((uint64_t)1 << s) - 1), halfway = (uint64_t)1 << (s - 1);
+    if (rem > halfway || (rem == halfway && (q & 1u))) q += 1u;
+    return (uint16_t)(sign | (uint16_t)q);
+}
+
+void oracle_f32_to_f16_array(size_t n, const float* x, uint16_t* y)
+{
+    for (size_t i = 0; i < n; ++i) y[i] = oracle_f32_to_f16_rne(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Reduction operators.                                                     */
+/* sum: IEEE binary32 add (round to nearest even).                          */
+/* max / min: IEEE 754-2019 maximumNumber / minimumNumber -- a NaN operand  */
+/* is ignored (NaN only if both are NaN), and -0 < +0.                      */
+/* The reduction over ranks is always a left fold in rank order 0..R-1.     */
+/* Pins: numpy fmax/fmin reductions on data without signed zeros; hand     */
+/* cases for the zero signs and NaN.                                        */
+/* ------------------------------------------------------------------------ */
+enum { ORACLE_SUM = 0, ORACLE_MAX = 1, ORACLE_MIN = 2 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+
+static int is_nan_f(float v) { return v != v; }
+static int sign_bit_f(float v) { uint32_t u; memcpy(&u, &v, sizeof u); return (int)(u >> 31); }
+
+float oracle_apply_op(int op, float a, float b)
+{
+    if (op == ORACLE_SUM) return a + b;
+    if (is_nan_f(a)) return b;
+    if (is_nan_f(b)) return a;
+    if (op == ORACLE_MAX) {
+        if (a > b) return a;
+        if (b > a) return b;
+        return sign_bit_f(a) ? b : a;                    /* equal: prefer +0 */
+    }
+    if (a < b) return a;
+    if (b < a) return b;
+    return sign_bit_f(a) ? a : b;                        /* equal: prefer -0 */
+}
+
+static float load_as_f32(int dtype, const void* x, size_t i)
+{
+    if (dtype == ORACLE_F32) return ((const float*)x)[i];
+    if (dtype == ORACLE_BF16) return oracle_bf16_to_f32(((const uint16_t*)x)[i]);
+    return oracle_f16_to_f32(((const uint16_t*)x)[i]);
+}
+
+static void store_from_f32(int dtype, void* y, size_t i, float v)
+{
+    if (dtype == ORACLE_F32) ((float*)y)[i] = v;
+    else if (dtype == ORACLE_BF16) ((uint16_t*)y)[i] = oracle_f32_to_bf16_rne(v);
+    else ((uint16_t*)y)[i] = oracle_f32_to_f16_rne(v);
+}
+
+/* AllReduce with any supported (dtype, op): widen exactly, fold in rank     */
+/* order in fp32, narrow once.  For (F32, SUM) and (BF16, SUM) this is the   */
+/* same arithmetic as the dedicated routines above.                          */
+void oracle_allreduce(int dtype, int op, int R, size_t n, const void* x, size_t ldx, void* y)
+{
+    for (size_t i = 0; i < n; ++i) {
+        float acc = load_as_f32(dtype, x, i);
+        for (int q = 1; q < R; ++q) {
+            acc = oracle_apply_op(op, acc, load_as_f32(dtype, x, (size_t)q * ldx + i));
+        }
+        store_from_f32(dtype, y, i, acc);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Threaded drivers (timing only).  The element range is split into equal   */
 /* contiguous parts, each handled by the same per-element routine above, so */
 /* results are identical to the single-threaded call.                       */
@@ -180,6 +298,29 @@ void oracle_allgather(int R, size_t S, const uint8_t* x, size_t ldx, uint8_t* y)
     for (int q = 0; q < R; ++q) {
         for (size_t i = 0; i < S; ++i) {
             y[(size_t)q * S + i] = x[(size_t)q * ldx + i];
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* AlltoAll.                                                                */
+/* [GIN] "pure GIN AlltoAll" example: every rank puts count elements to     */
+/* every rank r, taking them from its send buffer at r*count and placing    */
+/* them in r's receive buffer at my_rank*count; one signal increment per    */
+/* arriving put, the receiver waits for nRanks of them.  In bytes, with     */
+/* B = count*sizeof(T) per segment:                                         */
+/*     recv_p[q*B + i] = send_q[p*B + i]   for all ranks p, q and i < B.    */
+/* x: R rows of ldx bytes; y: R rows of ldy bytes.                          */
+/* Pins: the page's pattern my_rank*1000 + dest_rank*100 + element_idx;     */
+/* numpy transpose of the (sender, receiver) segment grid.                  */
+/* ------------------------------------------------------------------------ */
+void oracle_alltoall(int R, size_t B, const uint8_t* x, size_t ldx, uint8_t* y, size_t ldy)
+{
+    for (int p = 0; p < R; ++p) {
+        for (int q = 0; q < R; ++q) {
+            for (size_t i = 0; i < B; ++i) {
+                y[(size_t)p * ldy + (size_t)q * B + i] = x[(size_t)q * ldx + (size_t)p * B + i];
+            }
         }
     }
 }

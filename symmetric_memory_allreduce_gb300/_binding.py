@@ -62,6 +62,7 @@ _SIGS = {
     "sym_allgather": ([P, P, sz, i32, i32, sz, u32, P], i32),
     "sym_allgather_put_signal": ([P, P, sz, sz, u32, P, u64, P], i32),
     "sym_put_signal": ([P, P, i32, i32, sz, sz, sz, u32, u32, P], i32),
+    "sym_alltoall": ([P, P, sz, i32, i32, u64, P], i32),
     "sym_signal": ([P, i32, u32, u64, P], i32),
     "sym_signal_wait": ([P, i32, u32, u64, i32, u64, P], i32),
     "sym_signal_read": ([P, i32, u32, i32, ctypes.POINTER(u64), P], i32),
@@ -236,6 +237,12 @@ def sym_allgather_put_signal(send, recv, bytes_per_rank: int, chunk_bytes: int =
     _check(_lib.sym_allgather_put_signal(_handle(send), _handle(recv), bytes_per_rank, chunk_bytes,
                                          chunks_per_signal, d_mismatch or None, timeout_ns,
                                          _stream(stream)), "sym_allgather_put_signal")
+
+
+def sym_alltoall(send, recv, count: int, dtype="f32", algo="auto", timeout_ns: int = 0,
+                 stream=None):
+    _check(_lib.sym_alltoall(_handle(send), _handle(recv), count, DTYPES.get(dtype, dtype),
+                             ALGOS.get(algo, algo), timeout_ns, _stream(stream)), "sym_alltoall")
 
 
 def sym_put_signal(src, dst, src_rank: int, peer: int, dst_off: int, src_off: int, nbytes: int,

@@ -1,441 +1,9 @@
-// AllReduce(sum) over R rank windows carved from one GPU's HBM.
-//
-// What is computed ([SYMEX] "NCCL symmetric memory windows", Example 1: every
-// rank calls AllReduce(send, recv, count, float, sum) and every element of
-// every recv buffer is the sum over ranks):
-//     recv_r[i] = ((send_0[i] + send_1[i]) + ...) + send_{R-1}[i]   for all r,
-// added in rank order 0..R-1 with IEEE round-to-nearest adds (no contraction,
-// no flush-to-zero), so fp32 results are bit-identical on every rank and to a
-// plain sequential sum.  bf16 is widened exactly, accumulated in fp32 and
-// rounded to nearest-even once.
-//
-// Three data movements, all hand-written, 16-byte vector accesses:
-//  * one-shot   -- every rank-slot r reads all R windows at a tile and writes
-//                  only recv_r ([LSA]: a peer's buffer is read directly with
-//                  loads at base + offset).  Work items are ordered tile-major,
-//                  slot-minor, so the R slots of a tile run side by side and
-//                  their repeated reads of the same lines are served by L2.
-//  * two-shot   -- rank-slot q owns chunk q (1/R of the elements, 16-byte
-//                  aligned).  Reduce-scatter: slot q loads chunk q from all R
-//                  windows and reduces it.  All-gather: slot q stores the
-//                  reduced chunk into every window (the store form of the
-//                  all-gather), so nothing is read back.  HBM traffic is the
-//                  floor for the emulation: every input read once, every
-//                  output written once.
-//  * two-shot pull -- the same reduce-scatter, but the reduced chunk is only
-//                  written to recv_q; slot q then publishes one flag per tile
-//                  (st.release.gpu = epoch) and every other slot r waits for
-//                  the flag (ld.acquire.gpu, bounded) and copies the tile from
-//                  recv_q into recv_r.  This is the per-chunk completion flag
-//                  plus acquire spin of [GDA] section 5.1, with the give-up
-//                  timeout of [GIN]'s barrier.  A split form runs the two
-//                  phases as two launches (the kernel boundary is the barrier).
-#include <cstdio>
-
-#include "symar_internal.cuh"
+// C ABI entry of the AllReduce: argument checks, chunk plan, algorithm choice,
+// and dispatch to the per-element-type launchers (allreduce_{f32,bf16,f16}.cu;
+// the kernels themselves are in allreduce_kernels.cuh).
+#include "allreduce_kernels.cuh"
 
 namespace symar {
-
-constexpr int kThreads = 256;
-constexpr int kPullU = 4;                                    // 16 KiB tiles
-static_assert(kThreads * kPullU * kVecBytes == 16384, "pull tile must match the flag tile");
-
-// ----------------------------------------------------------------- element traits
-
-struct F32T {
-    static constexpr int V = 4;       // elements per 16 bytes
-    __device__ __forceinline__ static void widen(const uint4& x, float (&f)[4]) {
-        f[0] = __uint_as_float(x.x);
-        f[1] = __uint_as_float(x.y);
-        f[2] = __uint_as_float(x.z);
-        f[3] = __uint_as_float(x.w);
-    }
-    __device__ __forceinline__ static uint4 narrow(const float (&f)[4]) {
-        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
-                          __float_as_uint(f[3]));
-    }
-    __device__ __forceinline__ static float load1(const char* p) {
-        return *reinterpret_cast<const float*>(p);
-    }
-    __device__ __forceinline__ static void store1(char* p, float v) {
-        *reinterpret_cast<float*>(p) = v;
-    }
-};
-
-struct BF16T {
-    static constexpr int V = 8;
-    // element 2k is the low half of word k (little endian)
-    __device__ __forceinline__ static void widen(const uint4& x, float (&f)[8]) {
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            f[2 * k] = __uint_as_float(w[k] << 16);
-            f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-        }
-    }
-    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-    __device__ __forceinline__ static uint4 narrow(const float (&f)[8]) {
-        return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
-                          pack2(f[6], f[7]));
-    }
-    __device__ __forceinline__ static float load1(const char* p) {
-        return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(p)) << 16);
-    }
-    __device__ __forceinline__ static void store1(char* p, float v) {
-        __nv_bfloat16 h = __float2bfloat16_rn(v);
-        *reinterpret_cast<uint16_t*>(p) = *reinterpret_cast<uint16_t*>(&h);
-    }
-};
-
-// ----------------------------------------------------------------- memory access flavours
-
-enum LoadKind { kLoadStream = 0, kLoadKeep = 1 };
-
-template <int K>
-__device__ __forceinline__ uint4 load16(const char* p) {
-    if (K == kLoadStream) return __ldcs(reinterpret_cast<const uint4*>(p));   // read once
-    return __ldcg(reinterpret_cast<const uint4*>(p));                        // L2, reused
-}
-
-__device__ __forceinline__ void store16_stream(char* p, uint4 v) {
-    __stcs(reinterpret_cast<uint4*>(p), v);
-}
-
-__device__ __forceinline__ void store16_keep(char* p, uint4 v) {
-    __stcg(reinterpret_cast<uint4*>(p), v);
-}
-
-// ----------------------------------------------------------------- kernel arguments
-
-struct ArArgs {
-    const char* send;
-    char* recv;
-    size_t sstride, rstride;
-    int R;
-    size_t nvec;             // whole 16-byte vectors per rank
-    size_t chunk_vec;        // vectors per rank-slot chunk (two-shot)
-    uint32_t tiles_per_chunk;
-    uint32_t ntile;          // one-shot: tiles over nvec
-    size_t tail_elem0;       // first element past the last whole vector
-    uint32_t tail_n;         // elements in the ragged tail (< V)
-    // pull two-shot
-    uint32_t* flags;
-    size_t flag_stride;
-    uint32_t epoch;
-    uint32_t lag;            // tile blocks between a reduce and its gathers
-    int mode;                // 0 fused, 1 reduce-scatter only, 2 all-gather only
-    uint32_t* status;
-    uint64_t timeout_ns;
-};
-
-// Sum of R 16-byte vectors (rank order) at vector indices idx[k] of every
-// window; loads are issued RB ranks at a time before any add, for memory-level
-// parallelism; adds are __fadd_rn in rank order.
-template <class T, int RB, int U, int LK>
-__device__ __forceinline__ void reduce_vectors(const char* send, size_t sstride, int R,
-                                               const size_t (&idx)[U], const bool (&ok)[U],
-                                               float (&acc)[U][T::V]) {
-    for (int r0 = 0; r0 < R; r0 += RB) {
-        uint4 buf[RB][U];
-#pragma unroll
-        for (int j = 0; j < RB; ++j) {
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                buf[j][k] = make_uint4(0, 0, 0, 0);
-                if (r0 + j < R && ok[k])
-                    buf[j][k] = load16<LK>(send + (size_t)(r0 + j) * sstride + idx[k] * kVecBytes);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < RB; ++j) {
-            if (r0 + j < R) {
-#pragma unroll
-                for (int k = 0; k < U; ++k) {
-                    float f[T::V];
-                    T::widen(buf[j][k], f);
-                    if (r0 + j == 0) {
-#pragma unroll
-                        for (int e = 0; e < T::V; ++e) acc[k][e] = f[e];
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < T::V; ++e) acc[k][e] = __fadd_rn(acc[k][e], f[e]);
-                    }
-                }
-            }
-        }
-    }
-}
-
-// Ragged tail (fewer than V elements past the last whole vector): element
-// e of the tail is reduced by thread e and written to every slot in `slots`.
-template <class T>
-__device__ __forceinline__ void reduce_tail(const ArArgs& a, int slot_lo, int slot_hi) {
-    const int e = threadIdx.x;
-    if ((uint32_t)e >= a.tail_n) return;
-    constexpr size_t es = 16 / T::V;
-    const size_t off = (a.tail_elem0 + e) * es;
-    float acc = T::load1(a.send + off);
-    for (int r = 1; r < a.R; ++r) acc = __fadd_rn(acc, T::load1(a.send + (size_t)r * a.sstride + off));
-    for (int r = slot_lo; r < slot_hi; ++r) T::store1(a.recv + (size_t)r * a.rstride + off, acc);
-}
-
-// ----------------------------------------------------------------- two-shot (store all-gather)
-
-template <class T, int RB, int U>
-__global__ void __launch_bounds__(kThreads) k_twoshot_st(ArArgs a) {
-    constexpr size_t TILEV = (size_t)kThreads * U;
-    const uint32_t items = (uint32_t)a.R * a.tiles_per_chunk;
-    for (uint32_t w = blockIdx.x; w < items; w += gridDim.x) {
-        const uint32_t q = w / a.tiles_per_chunk, t = w - q * a.tiles_per_chunk;
-        const size_t c0 = (size_t)q * a.chunk_vec;
-        const size_t c1 = min(c0 + a.chunk_vec, a.nvec);
-        const size_t v0 = c0 + (size_t)t * TILEV;
-        if (v0 >= c1) continue;
-        size_t idx[U];
-        bool ok[U];
-#pragma unroll
-        for (int k = 0; k < U; ++k) {
-            idx[k] = v0 + threadIdx.x + (size_t)k * kThreads;
-            ok[k] = idx[k] < c1;
-        }
-        float acc[U][T::V];
-        reduce_vectors<T, RB, U, kLoadStream>(a.send, a.sstride, a.R, idx, ok, acc);
-        uint4 out[U];
-#pragma unroll
-        for (int k = 0; k < U; ++k) out[k] = T::narrow(acc[k]);
-        // all-gather by stores: slot q writes its reduced chunk into every window
-        for (int r = 0; r < a.R; ++r) {
-            char* dst = a.recv + (size_t)r * a.rstride;
-#pragma unroll
-            for (int k = 0; k < U; ++k)
-                if (ok[k]) store16_stream(dst + idx[k] * kVecBytes, out[k]);
-        }
-    }
-    if (a.tail_n && blockIdx.x == gridDim.x - 1) reduce_tail<T>(a, 0, a.R);
-}
-
-// ----------------------------------------------------------------- one-shot
-
-template <class T, int RB, int U>
-__global__ void __launch_bounds__(kThreads) k_oneshot(ArArgs a) {
-    constexpr size_t TILEV = (size_t)kThreads * U;
-    const uint32_t items = (uint32_t)a.R * a.ntile;
-    for (uint32_t w = blockIdx.x; w < items; w += gridDim.x) {
-        const uint32_t t = w / (uint32_t)a.R, r = w - t * (uint32_t)a.R;   // slot-minor
-        const size_t v0 = (size_t)t * TILEV;
-        size_t idx[U];
-        bool ok[U];
-#pragma unroll
-        for (int k = 0; k < U; ++k) {
-            idx[k] = v0 + threadIdx.x + (size_t)k * kThreads;
-            ok[k] = idx[k] < a.nvec;
-        }
-        float acc[U][T::V];
-        reduce_vectors<T, RB, U, kLoadKeep>(a.send, a.sstride, a.R, idx, ok, acc);
-        char* dst = a.recv + (size_t)r * a.rstride;
-#pragma unroll
-        for (int k = 0; k < U; ++k)
-            if (ok[k]) store16_stream(dst + idx[k] * kVecBytes, T::narrow(acc[k]));
-    }
-    if (a.tail_n && blockIdx.x == gridDim.x - 1) {
-        for (int r = 0; r < a.R; ++r) reduce_tail<T>(a, r, r + 1);   // each slot its own
-    }
-}
-
-// ----------------------------------------------------------------- two-shot (pull all-gather)
-
-template <class T, int RB>
-__device__ __forceinline__ void pull_reduce_item(const ArArgs& a, uint32_t q, uint32_t t) {
-    constexpr int U = kPullU;
-    constexpr size_t TILEV = (size_t)kThreads * U;
-    const size_t c0 = (size_t)q * a.chunk_vec;
-    const size_t c1 = min(c0 + a.chunk_vec, a.nvec);
-    const size_t v0 = c0 + (size_t)t * TILEV;
-    size_t idx[U];
-    bool ok[U];
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-        idx[k] = v0 + threadIdx.x + (size_t)k * kThreads;
-        ok[k] = idx[k] < c1;
-    }
-    float acc[U][T::V];
-    reduce_vectors<T, RB, U, kLoadStream>(a.send, a.sstride, a.R, idx, ok, acc);
-    char* dst = a.recv + (size_t)q * a.rstride;
-#pragma unroll
-    for (int k = 0; k < U; ++k)
-        if (ok[k]) store16_keep(dst + idx[k] * kVecBytes, T::narrow(acc[k]));
-}
-
-__device__ __forceinline__ void pull_copy_item(const ArArgs& a, uint32_t r, uint32_t q, uint32_t t) {
-    constexpr int U = kPullU;
-    constexpr size_t TILEV = (size_t)kThreads * U;
-    const size_t c0 = (size_t)q * a.chunk_vec;
-    const size_t c1 = min(c0 + a.chunk_vec, a.nvec);
-    const size_t v0 = c0 + (size_t)t * TILEV;
-    const char* src = a.recv + (size_t)q * a.rstride;
-    char* dst = a.recv + (size_t)r * a.rstride;
-    uint4 v[U];
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-        const size_t i = v0 + threadIdx.x + (size_t)k * kThreads;
-        if (i < c1) v[k] = __ldcg(reinterpret_cast<const uint4*>(src + i * kVecBytes));
-    }
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-        const size_t i = v0 + threadIdx.x + (size_t)k * kThreads;
-        if (i < c1) store16_stream(dst + i * kVecBytes, v[k]);
-    }
-}
-
-template <class T, int RB>
-__global__ void __launch_bounds__(kThreads) k_twoshot_pull(ArArgs a) {
-    constexpr size_t TILEV = (size_t)kThreads * kPullU;
-    __shared__ int s_ok[2];
-    const uint32_t R = (uint32_t)a.R, T_ = a.tiles_per_chunk;
-    const uint32_t RR = R * R;
-    uint32_t parity = 0;
-    auto tile_nonempty = [&](uint32_t q, uint32_t t) {
-        const size_t c0 = (size_t)q * a.chunk_vec;
-        return c0 + (size_t)t * TILEV < min(c0 + a.chunk_vec, a.nvec);
-    };
-    if (a.mode == 1) {                                   // reduce-scatter launch
-        for (uint32_t w = blockIdx.x; w < R * T_; w += gridDim.x) {
-            const uint32_t q = w / T_, t = w - q * T_;
-            if (tile_nonempty(q, t)) pull_reduce_item<T, RB>(a, q, t);
-        }
-        if (a.tail_n && blockIdx.x == gridDim.x - 1) reduce_tail<T>(a, 0, a.R);
-        return;
-    }
-    if (a.mode == 2) {                                   // all-gather launch
-        const uint32_t items = (R - 1) * R * T_;
-        for (uint32_t w = blockIdx.x; w < items; w += gridDim.x) {
-            const uint32_t qt = w / (R - 1), j = w - qt * (R - 1);
-            const uint32_t q = qt / T_, t = qt - q * T_;
-            const uint32_t r = j < q ? j : j + 1;
-            if (tile_nonempty(q, t)) pull_copy_item(a, r, q, t);
-        }
-        return;
-    }
-    // fused: slot sequence in blocks of R*R; block b holds the reduce items of
-    // tile b and the gather items of tile b - lag.
-    const uint64_t total = (uint64_t)(T_ + a.lag) * RR;
-    for (uint64_t w = blockIdx.x; w < total; w += gridDim.x) {
-        const uint32_t b = (uint32_t)(w / RR), s = (uint32_t)(w - (uint64_t)b * RR);
-        if (s < R) {
-            const uint32_t q = s, t = b;
-            if (t >= T_ || !tile_nonempty(q, t)) continue;
-            pull_reduce_item<T, RB>(a, q, t);
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                __threadfence();
-                st_release_u32(a.flags + (size_t)q * a.flag_stride + t, a.epoch);
-            }
-        } else {
-            if (b < a.lag) continue;
-            const uint32_t t = b - a.lag;
-            if (t >= T_) continue;
-            const uint32_t g = s - R, r = g / (R - 1), j = g - r * (R - 1);
-            const uint32_t q = j < r ? j : j + 1;
-            if (!tile_nonempty(q, t)) continue;
-            if (threadIdx.x == 0) {
-                const uint32_t* f = a.flags + (size_t)q * a.flag_stride + t;
-                const uint32_t ep = a.epoch;
-                bool got = bounded_spin([&] { return ld_acquire_u32(f) == ep; }, a.timeout_ns,
-                                        a.status);
-                if (!got) report_timeout(a.status, kSitePullFlag, q, t);
-                s_ok[parity] = got ? 1 : 0;
-            }
-            __syncthreads();
-            const bool go = s_ok[parity] != 0;
-            parity ^= 1u;
-            if (go) pull_copy_item(a, r, q, t);
-        }
-    }
-    if (a.tail_n && blockIdx.x == gridDim.x - 1) reduce_tail<T>(a, 0, a.R);
-}
-
-// ----------------------------------------------------------------- host dispatch
-
-template <class T>
-static sym_status_t launch_algo(sym_algo_t algo, ArArgs& a, sym_win_t recv, cudaStream_t st) {
-    DevCtx* ctx = recv->ctx;
-    const int sms = ctx->num_sms;
-    const bool wide = a.R > 4;
-    void (*kst)(ArArgs) = wide ? k_twoshot_st<T, 8, 2> : k_twoshot_st<T, 4, 2>;
-    void (*kone)(ArArgs) = wide ? k_oneshot<T, 8, 2> : k_oneshot<T, 4, 2>;
-    void (*kpull)(ArArgs) = wide ? k_twoshot_pull<T, 8> : k_twoshot_pull<T, 4>;
-    constexpr size_t TILEV2 = (size_t)kThreads * 2, TILEVP = (size_t)kThreads * kPullU;
-    switch (algo) {
-        case SYM_ALGO_ONESHOT: {
-            a.ntile = (uint32_t)ceil_div(a.nvec, TILEV2);
-            size_t items = (size_t)a.R * a.ntile;
-            int occ = occupancy((const void*)kone, kThreads, 0);
-            size_t grid = std::min(std::max(items, (size_t)1), (size_t)occ * sms);
-            kone<<<(unsigned)grid, kThreads, 0, st>>>(a);
-            count_launch();
-            break;
-        }
-        case SYM_ALGO_TWOSHOT: {
-            a.tiles_per_chunk = (uint32_t)ceil_div(a.chunk_vec, TILEV2);
-            size_t items = (size_t)a.R * a.tiles_per_chunk;
-            int occ = occupancy((const void*)kst, kThreads, 0);
-            size_t grid = std::min(std::max(items, (size_t)1), (size_t)occ * sms);
-            kst<<<(unsigned)grid, kThreads, 0, st>>>(a);
-            count_launch();
-            break;
-        }
-        case SYM_ALGO_TWOSHOT_PULL:
-        case SYM_ALGO_TWOSHOT_SPLIT: {
-            a.tiles_per_chunk = (uint32_t)ceil_div(a.chunk_vec, TILEVP);
-            if (a.tiles_per_chunk > recv->flag_tiles) return SYM_ERR_INVALID_ARG;
-            a.flags = recv->flags;
-            a.flag_stride = recv->flag_tiles;
-            a.status = ctx->status;
-            a.timeout_ns = default_timeout_ns();
-            int occ = occupancy((const void*)kpull, kThreads, 0);
-            size_t cap = (size_t)occ * sms;
-            if (algo == SYM_ALGO_TWOSHOT_SPLIT || a.R == 1) {
-                size_t rs = std::max((size_t)a.R * a.tiles_per_chunk, (size_t)1);
-                a.mode = 1;
-                kpull<<<(unsigned)std::min(rs, cap), kThreads, 0, st>>>(a);
-                count_launch();
-                if (a.R > 1 && a.tiles_per_chunk > 0) {
-                    size_t ag = (size_t)(a.R - 1) * a.R * a.tiles_per_chunk;
-                    a.mode = 2;
-                    kpull<<<(unsigned)std::min(ag, cap), kThreads, 0, st>>>(a);
-                    count_launch();
-                }
-                break;
-            }
-            // fused: blocks wait on one another -> co-residency via a cooperative launch
-            if (++recv->epoch == 0) {
-                SYM_CUDA(cudaMemsetAsync(recv->flags, 0,
-                                         sizeof(uint32_t) * recv->flag_tiles * recv->R, st));
-                recv->epoch = 1;
-            }
-            a.epoch = recv->epoch;
-            a.mode = 0;
-            size_t slots = (size_t)a.R * a.R * a.tiles_per_chunk;
-            size_t grid = std::min(std::max(slots, (size_t)1), cap);
-            a.lag = (uint32_t)ceil_div(grid, (size_t)a.R * a.R) + 1;
-            void* args[] = {&a};
-            SYM_CUDA(cudaLaunchCooperativeKernel((const void*)kpull, dim3((unsigned)grid),
-                                                 dim3(kThreads), args, 0, st));
-            count_launch();
-            break;
-        }
-        default:
-            return SYM_ERR_INVALID_ARG;
-    }
-    if (trace_on())
-        fprintf(stderr, "[symar] allreduce algo=%d R=%d nvec=%zu tail=%u\n", (int)algo, a.R, a.nvec,
-                a.tail_n);
-    SYM_CUDA(cudaGetLastError());
-    return SYM_OK;
-}
 
 static sym_algo_t resolve_algo(sym_algo_t algo, size_t nbytes, bool in_place) {
     if (algo != SYM_ALGO_AUTO) return algo;
@@ -466,10 +34,10 @@ sym_status_t sym_allreduce(sym_win_t send, sym_win_t recv, size_t count, sym_dty
     if ((int)op < SYM_SUM || (int)op > SYM_MIN) return SYM_ERR_INVALID_ARG;
     if ((int)algo < SYM_ALGO_AUTO || (int)algo > SYM_ALGO_TWOSHOT_SPLIT) return SYM_ERR_INVALID_ARG;
     if (count > send->bytes / es || count > recv->bytes / es) return SYM_ERR_INVALID_ARG;
-    if (op != SYM_SUM || dtype == SYM_F16) return SYM_ERR_UNSUPPORTED;
     if (count == 0) return SYM_OK;
     const bool in_place = send->base == recv->base;
     const size_t nbytes = count * es;
+    if (nbytes / kVecBytes > ((size_t)1 << 34)) return SYM_ERR_UNSUPPORTED;   // work-item indices
     algo = resolve_algo(algo, nbytes, in_place);
     if (in_place && algo == SYM_ALGO_ONESHOT) return SYM_ERR_UNSUPPORTED;
     if (in_place && send != recv) return SYM_ERR_INVALID_ARG;   // two handles, one memory
@@ -488,8 +56,12 @@ sym_status_t sym_allreduce(sym_win_t send, sym_win_t recv, size_t count, sym_dty
     DeviceGuard g(recv->device);
     if (!g.ok) return SYM_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
-    if (dtype == SYM_F32) return launch_algo<F32T>(algo, a, recv, st);
-    return launch_algo<BF16T>(algo, a, recv, st);
+    switch (dtype) {
+        case SYM_F32: return launch_allreduce_f32(algo, op, a, recv, st);
+        case SYM_BF16: return launch_allreduce_bf16(algo, op, a, recv, st);
+        case SYM_F16: return launch_allreduce_f16(algo, op, a, recv, st);
+    }
+    return SYM_ERR_INVALID_ARG;
 }
 
 }  // extern "C"

@@ -205,6 +205,59 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
     }
 }
 
+// ----------------------------------------------------------------- AlltoAll
+
+// [GIN] pure-GIN AlltoAll: sender q puts segment p of its send buffer into
+// rank p's receive buffer at segment q, with one signal increment per put;
+// the receiver waits for R increments.  Here one CTA moves one (q -> p)
+// segment, then (put+signal form) adds 1 to signal slot 0 of rank p.
+struct A2aArgs {
+    const char* send;
+    char* recv;
+    size_t sstride, rstride;
+    int R;
+    size_t B;                 // bytes per segment
+    int vec;
+    uint64_t* sig;            // recv window signals, slot 0 of each rank (put+signal form)
+    uint32_t nsig;
+    uint32_t nproducers;
+    uint32_t* status;
+    uint64_t timeout_ns;
+};
+
+__global__ void __launch_bounds__(kPutThreads) k_alltoall(A2aArgs a) {
+    const uint32_t R = (uint32_t)a.R, pairs = R * R;
+    if (blockIdx.x < a.nproducers) {
+        for (uint32_t pr = blockIdx.x; pr < pairs; pr += a.nproducers) {
+            const uint32_t q = pr / R, p = pr - q * R;
+            const char* src = a.send + (size_t)q * a.sstride + (size_t)p * a.B;
+            char* dst = a.recv + (size_t)p * a.rstride + (size_t)q * a.B;
+            block_copy<kPutThreads, kPutU>(src, dst, 0, a.B, a.vec != 0);
+            if (a.sig) {
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    red_release_add_u64(a.sig + (size_t)p * a.nsig, 1ull);
+                }
+            }
+        }
+    }
+    if (!a.sig) return;
+    // receivers: rank p waits until all R senders have signalled
+    for (uint32_t p = blockIdx.x; p < R; p += gridDim.x) {
+        if (threadIdx.x == 0) {
+            const uint64_t* sp = a.sig + (size_t)p * a.nsig;
+            if (!bounded_spin([&] { return ld_acquire_u64(sp) >= (uint64_t)R; }, a.timeout_ns,
+                              a.status))
+                report_timeout(a.status, kSitePutSignalRecv, p, 0xA2Au);
+        }
+    }
+}
+
+__global__ void k_reset_slot0(uint64_t* sig, uint32_t nsig, int R) {
+    for (int p = threadIdx.x; p < R; p += blockDim.x) sig[(size_t)p * nsig] = 0;
+}
+
 __global__ void k_reset_slots(uint64_t* sig, uint32_t nsig, uint64_t* cnt, uint32_t ncnt, int R) {
     for (int i = threadIdx.x; i < R * R; i += blockDim.x) {
         const int p = i / R, q = i - p * R;
@@ -384,6 +437,55 @@ sym_status_t sym_allgather_put_signal(sym_win_t send, sym_win_t recv, size_t byt
                                                  chunks_per_signal, d_mismatch, timeout_ns,
                                                  (cudaStream_t)stream);
     if (s != SYM_OK) return s;
+    SYM_CUDA(cudaGetLastError());
+    return SYM_OK;
+}
+
+sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtype_t dtype,
+                          sym_algo_t algo, uint64_t timeout_ns, sym_stream_t stream) {
+    if (!same_group(send, recv) || send == recv || send->base == recv->base)
+        return SYM_ERR_INVALID_ARG;
+    const size_t es = dtype_size(dtype);
+    if (!es) return SYM_ERR_INVALID_ARG;
+    if (algo != SYM_ALGO_AUTO && algo != SYM_ALGO_COPY && algo != SYM_ALGO_PUT_SIGNAL)
+        return SYM_ERR_INVALID_ARG;
+    const int R = send->R;
+    if (count > send->bytes / es / (size_t)R || count > recv->bytes / es / (size_t)R)
+        return SYM_ERR_INVALID_ARG;
+    const bool signalled = algo == SYM_ALGO_PUT_SIGNAL;
+    if (signalled && recv->nsignals < 1) return SYM_ERR_INVALID_ARG;
+    if (count == 0) return SYM_OK;
+    DeviceGuard g(recv->device);
+    if (!g.ok) return SYM_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    A2aArgs a{};
+    a.send = send->base;
+    a.recv = recv->base;
+    a.sstride = send->stride;
+    a.rstride = recv->stride;
+    a.R = R;
+    a.B = count * es;
+    a.vec = a.B % 16 == 0 ? 1 : 0;
+    a.status = recv->ctx->status;
+    a.timeout_ns = timeout_ns ? std::min(timeout_ns, (uint64_t)60000000000ull) : default_timeout_ns();
+    const size_t pairs = (size_t)R * R;
+    const int occ = occupancy((const void*)k_alltoall, kPutThreads, 0);
+    const size_t cap = (size_t)occ * recv->ctx->num_sms;
+    if (signalled) {
+        a.sig = recv->sig;
+        a.nsig = recv->nsignals;
+        k_reset_slot0<<<1, 64, 0, st>>>(a.sig, a.nsig, R);
+        count_launch();
+        a.nproducers = (uint32_t)std::min(pairs, cap);
+        void* args[] = {&a};
+        // receivers wait on senders of the same launch -> co-residency required
+        SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_alltoall, dim3(a.nproducers),
+                                             dim3(kPutThreads), args, 0, st));
+    } else {
+        a.nproducers = (uint32_t)std::min(pairs, cap);
+        k_alltoall<<<a.nproducers, kPutThreads, 0, st>>>(a);
+    }
+    count_launch();
     SYM_CUDA(cudaGetLastError());
     return SYM_OK;
 }

@@ -16,6 +16,7 @@ namespace symar {
 constexpr int kMaxRanks = 64;
 constexpr size_t kWindowAlign = 4096;        // window stride granularity
 constexpr int kVecBytes = 16;                // one 128-bit access
+constexpr size_t kPullTileBytes = 16384;     // pull two-shot: bytes of a chunk per flag
 
 // Device status word bits (DevCtx::status[0]).
 constexpr uint32_t kStatusTimeout = 1u;      // a bounded wait ran out
@@ -28,6 +29,7 @@ enum WaitSite : uint32_t {
     kSiteCounterWait = 2,
     kSitePullFlag = 3,
     kSitePutSignalRecv = 4,
+    kSiteBulkStage = 5,
 };
 
 // Per-device context: the status block and the arrival ring used by
@@ -86,6 +88,7 @@ void count_launch(int n = 1);          // sym_launch_count bookkeeping
 bool trace_on();
 uint64_t default_timeout_ns();
 size_t oneshot_max_bytes();
+bool twoshot_use_bulk();          // env SYM_TWOSHOT_KERNEL=bulk|ldst
 int occupancy(const void* kernel, int threads, size_t smem);   // blocks per SM, cached
 size_t dtype_size(sym_dtype_t t);       // 0 if unknown
 
@@ -165,8 +168,74 @@ __device__ __forceinline__ bool bounded_spin(Pred pred, uint64_t timeout_ns,
     return false;
 }
 
-// ----------------------------------------------------------------- launchers
+// ----------------------------------------------------------------- bulk async copies (TMA engine)
+//
+// Untiled cp.async.bulk: both addresses 16-byte aligned, size a multiple of 16.
+// Loads complete on an mbarrier (transaction bytes); stores complete in bulk
+// groups (commit / wait_group).
 
-struct ArPlan;   // defined in allreduce.cu
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 }  // namespace symar

@@ -73,6 +73,14 @@ size_t oneshot_max_bytes() {
     return v;
 }
 
+bool twoshot_use_bulk() {
+    static const bool v = [] {
+        const char* s = getenv("SYM_TWOSHOT_KERNEL");
+        return s && strcmp(s, "bulk") == 0;
+    }();
+    return v;
+}
+
 size_t dtype_size(sym_dtype_t t) {
     switch (t) {
         case SYM_F32: return 4;
@@ -131,10 +139,9 @@ using namespace symar;
 
 // Slot arrays and flags for a window: one allocation, zeroed.
 static sym_status_t alloc_aux(sym_window* w) {
-    // pull two-shot: one flag per (rank-slot, tile); a tile is 16 KiB of a chunk
-    const size_t tile_bytes = 16384;
+    // pull two-shot: one flag per (rank-slot, tile) of a chunk
     size_t chunk_bytes = ceil_div(ceil_div(w->bytes, (size_t)kVecBytes), (size_t)w->R) * kVecBytes;
-    w->flag_tiles = ceil_div(chunk_bytes, tile_bytes) + 1;
+    w->flag_tiles = ceil_div(chunk_bytes, kPullTileBytes) + 1;
     size_t sig_b = sizeof(uint64_t) * (size_t)w->R * w->nsignals;
     size_t cnt_b = sizeof(uint64_t) * (size_t)w->R * w->ncounters;
     size_t flg_b = sizeof(uint32_t) * (size_t)w->R * w->flag_tiles;

@@ -14,15 +14,15 @@ pytestmark = pytest.mark.gpu
 ALGOS = ["oneshot", "twoshot", "twoshot_pull", "twoshot_split"]
 
 
-def _run(sm, x, dtype, algo, in_place=False, nsig=0):
-    """x: (R, n) float32 or uint16 (bf16 bits). Returns (R, n) results of every rank."""
+def _run(sm, x, dtype, algo, in_place=False, op="sum"):
+    """x: (R, n) float32 or uint16 (16-bit patterns). Returns (R, n) results of every rank."""
     R, n = x.shape
     es = x.itemsize
     send = sm.Window(R, max(n * es, 16))
     recv = send if in_place else sm.Window(R, max(n * es, 16))
     try:
         upload(send, x)
-        sm.sym_allreduce(send, recv, n, dtype, "sum", algo)
+        sm.sym_allreduce(send, recv, n, dtype, op, algo)
         assert sm.sym_stream_status() == sm.SYM_OK
         return download(recv, n * es, x.dtype)
     finally:
@@ -136,6 +136,54 @@ def test_special_values(symar, oracle):
                               np.broadcast_to(want[~nan].view(np.uint32), y[:, ~nan].shape))
 
 
+def _half_inputs(dtype, f):
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    if dtype == "f32":
+        return f
+    if dtype == "bf16":
+        return wl.to_bf16_bits(f)
+    return np.ascontiguousarray(f.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
+@pytest.mark.parametrize("algo", ALGOS)
+def test_dtypes_and_ops(symar, oracle, dtype, op, algo):
+    """Every (dtype, op) through every algorithm: widen, fold in rank order in fp32, narrow once."""
+    rng = np.random.default_rng(300)
+    for R, n in [(1, 9), (3, 4097), (8, 100_003), (16, 65_539)]:
+        f = rng.uniform(-2, 2, size=(R, n)).astype(np.float32)
+        f[:, ::97] = 0.0
+        f[R // 2, ::89] = -0.0
+        if op != "sum":
+            f[0, ::101] = np.nan
+        x = _half_inputs(dtype, f)
+        want = oracle.allreduce(x, dtype, op)
+        y = _run(symar, x, dtype, algo, op=op)
+        if dtype == "f32":
+            nan = np.isnan(want)
+            assert np.all(np.isnan(y[:, nan]))
+            assert np.array_equal(y[:, ~nan].view(np.uint32),
+                                  np.broadcast_to(want[~nan].view(np.uint32), y[:, ~nan].shape))
+        else:
+            nanbits = (want & 0x7FFF) > (0x7F80 if dtype == "bf16" else 0x7C00)
+            assert np.array_equal(y[:, ~nanbits], np.broadcast_to(want[~nanbits], y[:, ~nanbits].shape))
+
+
+def test_f16_rounding_edges(symar, oracle):
+    """fp16 sums that overflow to Inf, land on subnormals, or tie in rounding."""
+    R, n = 4, 4096
+    rng = np.random.default_rng(301)
+    f = np.empty((R, n), np.float32)
+    f[:] = rng.choice([65504.0, 30000.0, 2.0 ** -24, 2.0 ** -15, 1.0, 2.0 ** -11, -65504.0],
+                      size=(R, n)).astype(np.float32)
+    x = _half_inputs("f16", f)
+    for algo in ALGOS:
+        want = oracle.allreduce(x, "f16", "sum")
+        assert np.array_equal(_run(symar, x, "f16", algo), np.broadcast_to(want, (R, n)))
+
+
 def test_zero_count_and_validation(symar):
     a, b = symar.Window(4, 4096), symar.Window(8, 4096)
     try:
@@ -149,8 +197,8 @@ def test_zero_count_and_validation(symar):
                 bad()
             assert e.value.status == symar.SYM_ERR_INVALID_ARG
         with pytest.raises(symar.SymError) as e:
-            symar.sym_allreduce(a, a, 16, "f32", "max", "twoshot")
-        assert e.value.status == symar.SYM_ERR_UNSUPPORTED
+            symar.sym_allreduce(a, a, 16, "f32", 7, "twoshot")             # unknown op
+        assert e.value.status == symar.SYM_ERR_INVALID_ARG
     finally:
         a.free()
         b.free()

@@ -312,3 +312,159 @@ def test_rolling_le_truth_table(oracle):
         assert oracle.rolling_le(x, x)
     assert oracle.read_bits(2**60 + 5, 56) == 5
     assert oracle.read_bits(M, 64) == M
+
+
+# ---------------------------------------------------------------- fp16 rounding
+
+def _np_f16_bits(f32):
+    return np.ascontiguousarray(f32, np.float32).astype(np.float16).view(np.uint16)
+
+
+def test_f16_hand_cases(oracle):
+    cases = {
+        1.0: 0x3C00, 65504.0: 0x7BFF, 65519.99: 0x7BFF, 65520.0: 0x7C00, 1e6: 0x7C00,
+        -2.0: 0xC000, 2.0 ** -14: 0x0400, 2.0 ** -24: 0x0001, 2.0 ** -25: 0x0000,   # tie -> even 0
+        3 * 2.0 ** -25: 0x0002,                                                   # tie -> even 2
+        1.0 + 2.0 ** -11: 0x3C00,                                                 # tie -> even
+        1.0 + 3 * 2.0 ** -11: 0x3C02, float("inf"): 0x7C00, -0.0: 0x8000,
+        2.0 ** -15 * (1 + 2.0 ** -10): 0x0200,
+    }
+    for v, h in cases.items():
+        assert oracle.f32_to_f16(np.array([v], np.float32))[0] == h, v
+    assert oracle.f32_to_f16(np.array([np.nan], np.float32))[0] == 0x7E00
+
+
+def test_f16_rounding_matches_numpy_stratified(oracle):
+    hi = np.arange(1 << 16, dtype=np.uint32) << 16
+    lows = np.array([0, 1, 0x0FFF, 0x1000, 0x1001, 0x7FFF, 0x8000, 0xFFFF], np.uint32)
+    u = (hi[:, None] | lows[None, :]).ravel()
+    rng = np.random.default_rng(17)
+    u = np.concatenate([u, rng.integers(0, 2**32, size=1 << 20, dtype=np.uint64).astype(np.uint32)])
+    f = u.view(np.float32)
+    ok = ~np.isnan(f)
+    with np.errstate(over="ignore"):
+        ref = _np_f16_bits(f)
+    assert np.array_equal(oracle.f32_to_f16(f)[ok], ref[ok])
+
+
+def _f16_value(h):
+    s = -1 if h & 0x8000 else 1
+    e = (h >> 10) & 0x1F
+    m = h & 0x3FF
+    if e == 0:
+        return s * Fraction(m, 1 << 24)
+    return s * (1 + Fraction(m, 1024)) * Fraction(2) ** (e - 15)
+
+
+def test_f16_brute_force_nearest(oracle):
+    """Exact rationals over every finite half: the nearest half, ties to even."""
+    rng = np.random.default_rng(19)
+    vals = rng.uniform(-70000, 70000, 1500).astype(np.float32)
+    vals = np.concatenate([vals, (rng.uniform(-1, 1, 1500) * 2.0 ** -13).astype(np.float32)])
+    halves = [h for h in range(0x7C00)]
+    grid = sorted((_f16_value(h), h) for h in halves)
+    import bisect
+    keys = [g[0] for g in grid]
+    for v in vals:
+        ex = Fraction(float(v))
+        a = abs(ex)
+        if a >= Fraction(65520):
+            want = 0x7C00
+        else:
+            i = bisect.bisect_left(keys, a)
+            cands = [grid[j] for j in (i - 1, i) if 0 <= j < len(grid)]
+            best = min(abs(c[0] - a) for c in cands)
+            near = [c for c in cands if abs(c[0] - a) == best]
+            want = near[0][1] if len(near) == 1 else [c for c in near if c[1] % 2 == 0][0][1]
+        if v < 0 or (v == 0 and np.signbit(v)):
+            want |= 0x8000
+        assert oracle.f32_to_f16(np.array([v]))[0] == want, float(v)
+
+
+def test_f16_widen_exact(oracle):
+    for h in list(range(0, 0x7C01, 7)) + [0x0001, 0x03FF, 0x0400, 0x7BFF, 0x8001, 0xFBFF]:
+        f = oracle.f16_to_f32_scalar(h)
+        assert float(np.array([h], np.uint16).view(np.float16)[0]) == f or (np.isnan(f))
+
+
+# ---------------------------------------------------------------- reduction operators
+
+def test_max_min_against_numpy(oracle):
+    rng = np.random.default_rng(23)
+    for R in (1, 2, 3, 8):
+        x = rng.standard_normal((R, 999)).astype(np.float32)
+        x[rng.random(x.shape) < 0.05] = np.nan
+        for op, ref in (("max", np.fmax), ("min", np.fmin)):
+            want = ref.reduce(x, axis=0)
+            got = oracle.allreduce(x, "f32", op)
+            assert np.array_equal(np.isnan(got), np.isnan(want))
+            m = ~np.isnan(want)
+            assert np.array_equal(got[m], want[m])
+
+
+def test_max_min_zero_signs_and_nan(oracle):
+    nan = float("nan")
+    assert np.signbit(oracle.apply_op("max", -0.0, 0.0)) == False      # noqa: E712
+    assert np.signbit(oracle.apply_op("max", 0.0, -0.0)) == False      # noqa: E712
+    assert np.signbit(oracle.apply_op("min", 0.0, -0.0)) == True       # noqa: E712
+    assert np.signbit(oracle.apply_op("min", -0.0, 0.0)) == True       # noqa: E712
+    assert oracle.apply_op("max", nan, 2.0) == 2.0
+    assert oracle.apply_op("min", 2.0, nan) == 2.0
+    assert math.isnan(oracle.apply_op("max", nan, nan))
+    assert oracle.apply_op("sum", 1e8, 1.0) == np.float32(1e8)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
+def test_half_types_generic_allreduce(oracle, dtype, op):
+    """Widen, fold in fp32 in rank order, narrow once -- checked with numpy/torch primitives."""
+    rng = np.random.default_rng(29)
+    R, n = 5, 513
+    f = rng.uniform(-3, 3, size=(R, n)).astype(np.float32)
+    if dtype == "bf16":
+        x = _torch_bf16_bits(f).reshape(R, n)
+        wide = (x.astype(np.uint32) << 16).view(np.float32)
+    else:
+        x = _np_f16_bits(f).reshape(R, n)
+        wide = x.view(np.float16).astype(np.float32)
+    if op == "sum":
+        acc = _seq_sum_np(wide)
+    else:
+        acc = (np.fmax if op == "max" else np.fmin).reduce(wide, axis=0)
+    want = _torch_bf16_bits(acc) if dtype == "bf16" else _np_f16_bits(acc)
+    assert np.array_equal(oracle.allreduce(x, dtype, op), want)
+
+
+def test_generic_matches_dedicated(oracle):
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((7, 3001)).astype(np.float32)
+    assert np.array_equal(oracle.allreduce(x, "f32", "sum").view(np.uint32),
+                          oracle.allreduce_sum_f32(x).view(np.uint32))
+    xb = oracle.f32_to_bf16(x).reshape(x.shape)
+    assert np.array_equal(oracle.allreduce(xb, "bf16", "sum"), oracle.allreduce_sum_bf16(xb))
+
+
+# ---------------------------------------------------------------- AlltoAll
+
+def test_alltoall_gin_pattern(oracle):
+    """GIN page's AlltoAll example: value = my_rank*1000 + dest_rank*100 + element_idx."""
+    g = open(os.path.join(GOLDEN, "alltoall_pattern.txt")).read()
+    assert "my_rank*1000+dest_rank*100+element_idx" in g
+    R, count = 4, 64
+    send = np.empty((R, R * count), np.float32)
+    for q in range(R):                       # q = my_rank (sender)
+        for p in range(R):                   # p = dest_rank
+            send[q, p * count:(p + 1) * count] = q * 1000 + p * 100 + np.arange(count)
+    recv = oracle.alltoall(send.view(np.uint8)).view(np.float32)
+    for p in range(R):                       # receiver
+        for q in range(R):                   # segment from sender q
+            assert np.array_equal(recv[p, q * count:(q + 1) * count],
+                                  q * 1000 + p * 100 + np.arange(count, dtype=np.float32))
+
+
+@pytest.mark.parametrize("R,B", [(1, 7), (3, 16), (16, 100), (5, 0)])
+def test_alltoall_transpose(oracle, R, B):
+    rng = np.random.default_rng(R * 10 + B)
+    x = rng.integers(0, 256, size=(R, R * B), dtype=np.uint8)
+    want = x.reshape(R, R, B).transpose(1, 0, 2).reshape(R, R * B)
+    assert np.array_equal(oracle.alltoall(x), want)

@@ -240,3 +240,47 @@ def test_counter_56_bits(symar):
     finally:
         src.free()
         dst.free()
+
+
+@pytest.mark.parametrize("algo", ["copy", "put_signal"])
+def test_alltoall_gin_pattern(symar, oracle, algo):
+    """The GIN page's AlltoAll check: rank p finds my_rank*1000 + dest_rank*100 + idx from q."""
+    R, count = 8, 4096 + 3
+    send_h = np.empty((R, R * count), np.float32)
+    for q in range(R):
+        for p in range(R):
+            send_h[q, p * count:(p + 1) * count] = q * 1000 + p * 100 + np.arange(count)
+    send, recv = symar.Window(R, R * count * 4), symar.Window(R, R * count * 4, nsignals=1)
+    try:
+        upload(send, send_h)
+        symar.sym_alltoall(send, recv, count, "f32", algo)
+        assert symar.sym_stream_status() == symar.SYM_OK
+        got = download(recv, R * count * 4, np.float32)
+        for p in range(R):
+            for q in range(R):
+                assert np.array_equal(got[p, q * count:(q + 1) * count],
+                                      q * 1000 + p * 100 + np.arange(count, dtype=np.float32))
+        assert np.array_equal(got.view(np.uint8), oracle.alltoall(send_h.view(np.uint8)))
+        if algo == "put_signal":
+            assert all(symar.sym_signal_read(recv, p, 0) == R for p in range(R))
+    finally:
+        send.free()
+        recv.free()
+
+
+@pytest.mark.parametrize("R,B", [(1, 16), (3, 6), (16, 65536), (5, 1000)])
+def test_alltoall_random(symar, oracle, R, B):
+    rng = np.random.default_rng(R + B)
+    x = rng.integers(0, 256, size=(R, R * B), dtype=np.uint8)
+    send, recv = symar.Window(R, R * B), symar.Window(R, R * B, nsignals=2)
+    try:
+        upload(send, x)
+        es = 4 if B % 4 == 0 else 2
+        for algo in ("copy", "put_signal"):
+            recv.tensor().zero_()
+            symar.sym_alltoall(send, recv, B // es, "f32" if es == 4 else "bf16", algo)
+            assert symar.sym_stream_status() == symar.SYM_OK
+            assert np.array_equal(download(recv, R * B), oracle.alltoall(x))
+    finally:
+        send.free()
+        recv.free()
