@@ -78,7 +78,8 @@ typedef enum {
     SYM_ALGO_TWOSHOT_SPLIT = 4,  /* reduce-scatter launch, then pull all-gather launch */
     /* AllGather */
     SYM_ALGO_COPY = 5,           /* read each segment once, store it to all R ranks */
-    SYM_ALGO_PUT_SIGNAL = 6      /* chunked puts, one strong signal per batch, receivers wait */
+    SYM_ALGO_PUT_SIGNAL = 6,     /* chunked puts, one strong signal per batch, receivers wait */
+    SYM_ALGO_CE = 7              /* copy engines, no kernel: one 2-D memcpy per destination */
 } sym_algo_t;
 
 /* ---------------------------------------------------------------- windows */
@@ -150,9 +151,12 @@ sym_status_t sym_allreduce_algo(sym_win_t send, size_t count, sym_dtype_t dtype,
  * i < S = sendcount*sizeof(dtype).  [SYMEX] Example 2: the receive buffer
  * holds sendcount*nranks elements and segment q holds rank q's data.
  * recv bytes_per_rank >= R*S.  send and recv must be different windows.
- * algo: AUTO or COPY, or PUT_SIGNAL (see sym_allgather_put_signal, with
- * chunk_bytes and chunks_per_signal; 0 selects 64 KiB and 8).  For COPY the
- * two chunk arguments are ignored. */
+ * algo: AUTO or COPY (SM kernel: each segment tile read once, stored R
+ * times), CE ([SYMEX] Example 2's copy-engine policy, CTAPolicy ZERO: no SM
+ * is used; one cudaMemcpy2DAsync per destination rank gathers the R
+ * segments), or PUT_SIGNAL (see sym_allgather_put_signal, with chunk_bytes
+ * and chunks_per_signal; 0 selects 64 KiB and 8).  For COPY and CE the two
+ * chunk arguments are ignored. */
 sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym_dtype_t dtype,
                            sym_algo_t algo, size_t chunk_bytes, uint32_t chunks_per_signal,
                            sym_stream_t stream);
@@ -196,6 +200,20 @@ sym_status_t sym_allgather_put_signal(sym_win_t send, sym_win_t recv, size_t byt
  * sym_stream_status(). */
 sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtype_t dtype,
                           sym_algo_t algo, uint64_t timeout_ns, sym_stream_t stream);
+
+/* Producer + AllReduce in one launch.  Every rank r first produces its
+ * contribution s_r[i] = alpha[r] * in_r[i] (one fp32 multiply, rounded to
+ * nearest) into `send`; then recv_r[i] = s_0[i] + s_1[i] + ... + s_{R-1}[i]
+ * (rank order, fp32) for every rank r.  [GDA] section 5.1 (fused GEMM +
+ * AllReduce): producer tiles bump a per-tile counter, the R-th arrival
+ * publishes the tile's flag with a release store, and the reduction of that
+ * tile starts as soon as it acquires the flag, overlapping the production of
+ * later tiles.  alpha: host array of R floats (copied at the call).  f32
+ * only; the three windows must have the same R and be distinct.  count
+ * elements per rank.  Errors: INVALID_ARG, UNSUPPORTED, CUDA; a wait that
+ * runs out -> SYM_ERR_TIMEOUT from sym_stream_status(). */
+sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_win_t recv, const float* alpha,
+                                 size_t count, sym_stream_t stream);
 
 /* ---------------------------------------------------------------- one-sided */
 

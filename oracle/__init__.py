@@ -170,6 +170,24 @@ def alltoall(x: np.ndarray) -> np.ndarray:
     return y
 
 
+def scale_allreduce(a: np.ndarray, alpha) -> tuple[np.ndarray, np.ndarray]:
+    """a: (R, N) float32, alpha: R floats -> (s (R, N) = alpha_r * a_r, y (N,) rank-order sum)."""
+    a = _rows(a, np.float32)
+    R, n = a.shape
+    al = np.ascontiguousarray(np.asarray(alpha, np.float32).ravel())
+    if al.size != R:
+        raise ValueError("one alpha per rank")
+    s = np.empty_like(a)
+    y = np.empty(n, np.float32)
+    lib = _load()
+    P, sz = ctypes.c_void_p, ctypes.c_size_t
+    lib.oracle_scale_allreduce.argtypes = [ctypes.c_int, sz, P, P, sz, P, sz, P]
+    lib.oracle_scale_allreduce.restype = None
+    if n:
+        lib.oracle_scale_allreduce(R, n, _ptr(al), _ptr(a), n, _ptr(s), n, _ptr(y))
+    return s, y
+
+
 def put_signal_allgather(x: np.ndarray, chunk: int, batch: int):
     """Sequential put+signal model. x: (R, S) uint8.
 

@@ -228,6 +228,29 @@ void oracle_allreduce(int dtype, int op, int R, size_t n, const void* x, size_t 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Producer + AllReduce.                                                    */
+/* [GDA] section 5.1: compute tiles produce each rank's contribution, and   */
+/* the AllReduce consumes it.  The producer here is one binary32 multiply   */
+/* per element, rounded to nearest:                                         */
+/*     s_r[i] = alpha_r * a_r[i]                                            */
+/* and the consumer is the fp32 AllReduce in rank order:                    */
+/*     y[i] = ((s_0[i] + s_1[i]) + ...) + s_{R-1}[i].                       */
+/* s: R rows of lds floats (the contributions), y: n floats.                */
+/* Pins: alpha = 1 gives the plain AllReduce; rank fill with alpha_r = r+1  */
+/* gives the closed form sum r(r+1); numpy float32 brute force.             */
+/* ------------------------------------------------------------------------ */
+void oracle_scale_allreduce(int R, size_t n, const float* alpha, const float* a, size_t lda,
+                            float* s, size_t lds, float* y)
+{
+    for (int q = 0; q < R; ++q) {
+        for (size_t i = 0; i < n; ++i) {
+            s[(size_t)q * lds + i] = alpha[q] * a[(size_t)q * lda + i];
+        }
+    }
+    oracle_allreduce_sum_f32(R, n, s, lds, y);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Threaded drivers (timing only).  The element range is split into equal   */
 /* contiguous parts, each handled by the same per-element routine above, so */
 /* results are identical to the single-threaded call.                       */

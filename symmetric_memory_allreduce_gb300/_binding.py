@@ -24,12 +24,12 @@ SYM_F32, SYM_BF16, SYM_F16 = 0, 1, 2
 SYM_SUM, SYM_MAX, SYM_MIN = 0, 1, 2
 SYM_ALGO_AUTO, SYM_ALGO_ONESHOT, SYM_ALGO_TWOSHOT = 0, 1, 2
 SYM_ALGO_TWOSHOT_PULL, SYM_ALGO_TWOSHOT_SPLIT = 3, 4
-SYM_ALGO_COPY, SYM_ALGO_PUT_SIGNAL = 5, 6
+SYM_ALGO_COPY, SYM_ALGO_PUT_SIGNAL, SYM_ALGO_CE = 5, 6, 7
 NO_ID = 0xFFFFFFFF
 
 ALGOS = {"auto": SYM_ALGO_AUTO, "oneshot": SYM_ALGO_ONESHOT, "twoshot": SYM_ALGO_TWOSHOT,
          "twoshot_pull": SYM_ALGO_TWOSHOT_PULL, "twoshot_split": SYM_ALGO_TWOSHOT_SPLIT,
-         "copy": SYM_ALGO_COPY, "put_signal": SYM_ALGO_PUT_SIGNAL}
+         "copy": SYM_ALGO_COPY, "put_signal": SYM_ALGO_PUT_SIGNAL, "ce": SYM_ALGO_CE}
 DTYPES = {"f32": SYM_F32, "bf16": SYM_BF16, "f16": SYM_F16}
 OPS = {"sum": SYM_SUM, "max": SYM_MAX, "min": SYM_MIN}
 
@@ -63,6 +63,7 @@ _SIGS = {
     "sym_allgather_put_signal": ([P, P, sz, sz, u32, P, u64, P], i32),
     "sym_put_signal": ([P, P, i32, i32, sz, sz, sz, u32, u32, P], i32),
     "sym_alltoall": ([P, P, sz, i32, i32, u64, P], i32),
+    "sym_scale_allreduce": ([P, P, P, P, sz, P], i32),
     "sym_signal": ([P, i32, u32, u64, P], i32),
     "sym_signal_wait": ([P, i32, u32, u64, i32, u64, P], i32),
     "sym_signal_read": ([P, i32, u32, i32, ctypes.POINTER(u64), P], i32),
@@ -243,6 +244,13 @@ def sym_alltoall(send, recv, count: int, dtype="f32", algo="auto", timeout_ns: i
                  stream=None):
     _check(_lib.sym_alltoall(_handle(send), _handle(recv), count, DTYPES.get(dtype, dtype),
                              ALGOS.get(algo, algo), timeout_ns, _stream(stream)), "sym_alltoall")
+
+
+def sym_scale_allreduce(inp, send, recv, alpha, count: int, stream=None):
+    """alpha: sequence of R floats (copied into the launch)."""
+    al = (ctypes.c_float * len(alpha))(*[float(v) for v in alpha])
+    _check(_lib.sym_scale_allreduce(_handle(inp), _handle(send), _handle(recv), al, count,
+                                    _stream(stream)), "sym_scale_allreduce")
 
 
 def sym_put_signal(src, dst, src_rank: int, peer: int, dst_off: int, src_off: int, nbytes: int,

@@ -1,0 +1,190 @@
+// Producer + AllReduce in one persistent launch, with per-tile counter relay.
+//
+// [GDA] section 5.1 (mKernel's fused GEMM + AllReduce): compute tiles bump a
+// per-chunk counter with atomicAdd; the tile that completes a chunk publishes
+// a flag with a release store; the reducing role spins on the flag with an
+// acquire load and a short sleep, then reduces.  Here the producer is one
+// binary32 multiply per element (each rank's contribution
+// s_r = alpha_r * a_r, written to the send window as a GEMM epilogue would),
+// and the consumer is the two-shot AllReduce by loads + stores over the
+// contributions.  A tile of the result is reduced as soon as the R producer
+// tiles it needs are in place, while other tiles are still being produced.
+#include "allreduce_kernels.cuh"
+
+namespace symar {
+
+struct FusedArgs {
+    const char* in;
+    char* send;
+    char* recv;
+    size_t istride, sstride, rstride;
+    int R;
+    size_t nvec, chunk_vec;
+    uint32_t tiles_per_chunk;
+    size_t tail_elem0;
+    uint32_t tail_n;
+    uint32_t* flags;
+    uint32_t* arrivals;
+    size_t flag_stride;
+    uint32_t epoch, lag;
+    uint32_t* status;
+    uint64_t timeout_ns;
+    float alpha[kMaxRanks];
+};
+
+// slot sequence in blocks of R*R + R: block b holds the producer items (r, q)
+// of tile b and the consumer items q of tile b - lag.
+__global__ void __launch_bounds__(kThreads) k_scale_allreduce(FusedArgs a) {
+    constexpr int U = kPullU;
+    constexpr size_t TILEV = (size_t)kThreads * U;
+    __shared__ int s_ok[2];
+    const uint32_t R = (uint32_t)a.R, T_ = a.tiles_per_chunk;
+    const uint32_t per_block = R * R + R;
+    uint32_t parity = 0;
+    const uint64_t total = (uint64_t)(T_ + a.lag) * per_block;
+    for (uint64_t w = blockIdx.x; w < total; w += gridDim.x) {
+        const uint32_t b = (uint32_t)(w / per_block), s = (uint32_t)(w - (uint64_t)b * per_block);
+        const bool producer = s < R * R;
+        const uint32_t t = producer ? b : b - a.lag;
+        if (!producer && b < a.lag) continue;
+        if (t >= T_) continue;
+        const uint32_t q = producer ? s % R : s - R * R;
+        const size_t c0 = (size_t)q * a.chunk_vec;
+        const size_t c1 = min(c0 + a.chunk_vec, a.nvec);
+        const size_t v0 = c0 + (size_t)t * TILEV;
+        if (v0 >= c1) continue;
+        size_t idx[U];
+        bool ok[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            idx[k] = v0 + threadIdx.x + (size_t)k * kThreads;
+            ok[k] = idx[k] < c1;
+        }
+        if (producer) {
+            const uint32_t r = s / R;
+            const float al = a.alpha[r];
+            const char* src = a.in + (size_t)r * a.istride;
+            char* dst = a.send + (size_t)r * a.sstride;
+            uint4 v[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k)
+                if (ok[k]) v[k] = __ldcs(reinterpret_cast<const uint4*>(src + idx[k] * kVecBytes));
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                if (!ok[k]) continue;
+                float f[4];
+                F32T::widen(v[k], f);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) f[e] = __fmul_rn(al, f[e]);
+                store16_keep(dst + idx[k] * kVecBytes, F32T::narrow(f));
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                uint32_t* cnt = a.arrivals + (size_t)q * a.flag_stride + t;
+                if (atomicAdd(cnt, 1u) == R - 1) {          // the last of the R producers
+                    *cnt = 0;
+                    __threadfence();
+                    st_release_u32(a.flags + (size_t)q * a.flag_stride + t, a.epoch);
+                }
+            }
+        } else {
+            if (threadIdx.x == 0) {
+                const uint32_t* f = a.flags + (size_t)q * a.flag_stride + t;
+                const uint32_t ep = a.epoch;
+                bool got = bounded_spin([&] { return ld_acquire_u32(f) == ep; }, a.timeout_ns,
+                                        a.status);
+                if (!got) report_timeout(a.status, kSitePullFlag, q, t);
+                s_ok[parity] = got ? 1 : 0;
+            }
+            __syncthreads();
+            const bool go = s_ok[parity] != 0;
+            parity ^= 1u;
+            if (!go) continue;
+            float acc[U][4];
+            if (a.R > 4)
+                reduce_vectors<F32T, OpSum, 8, U, kLoadKeep>(a.send, a.sstride, a.R, idx, ok, acc);
+            else
+                reduce_vectors<F32T, OpSum, 4, U, kLoadKeep>(a.send, a.sstride, a.R, idx, ok, acc);
+            uint4 out[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k) out[k] = F32T::narrow(acc[k]);
+            for (int r = 0; r < a.R; ++r) {
+                char* dst = a.recv + (size_t)r * a.rstride;
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    if (ok[k]) store16_stream(dst + idx[k] * kVecBytes, out[k]);
+            }
+        }
+    }
+    // ragged tail: this block produces and reduces it alone
+    if (a.tail_n && blockIdx.x == gridDim.x - 1 && threadIdx.x < a.tail_n) {
+        const size_t off = (a.tail_elem0 + threadIdx.x) * 4;
+        float acc = 0.f;
+        for (int r = 0; r < a.R; ++r) {
+            const float v = __fmul_rn(a.alpha[r], *reinterpret_cast<const float*>(a.in + (size_t)r * a.istride + off));
+            *reinterpret_cast<float*>(a.send + (size_t)r * a.sstride + off) = v;
+            acc = r == 0 ? v : __fadd_rn(acc, v);
+        }
+        for (int r = 0; r < a.R; ++r) *reinterpret_cast<float*>(a.recv + (size_t)r * a.rstride + off) = acc;
+    }
+}
+
+}  // namespace symar
+
+using namespace symar;
+
+extern "C" sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_win_t recv,
+                                            const float* alpha, size_t count, sym_stream_t stream) {
+    if (!in || !send || !recv || !alpha) return SYM_ERR_INVALID_ARG;
+    if (in->R != send->R || send->R != recv->R) return SYM_ERR_INVALID_ARG;
+    if (in->device != send->device || send->device != recv->device) return SYM_ERR_INVALID_ARG;
+    if (in->base == send->base || send->base == recv->base || in->base == recv->base)
+        return SYM_ERR_INVALID_ARG;
+    if (count > in->bytes / 4 || count > send->bytes / 4 || count > recv->bytes / 4)
+        return SYM_ERR_INVALID_ARG;
+    if (count == 0) return SYM_OK;
+    const size_t nbytes = count * 4;
+    if (nbytes / kVecBytes > ((size_t)1 << 34)) return SYM_ERR_UNSUPPORTED;
+    FusedArgs a{};
+    a.in = in->base;
+    a.send = send->base;
+    a.recv = recv->base;
+    a.istride = in->stride;
+    a.sstride = send->stride;
+    a.rstride = recv->stride;
+    a.R = recv->R;
+    a.nvec = nbytes / kVecBytes;
+    a.chunk_vec = ceil_div(a.nvec, (size_t)a.R);
+    a.tail_elem0 = a.nvec * 4;
+    a.tail_n = (uint32_t)(count - a.tail_elem0);
+    a.tiles_per_chunk = (uint32_t)ceil_div(a.chunk_vec, (size_t)kThreads * kPullU);
+    if (a.tiles_per_chunk > recv->flag_tiles) return SYM_ERR_INVALID_ARG;
+    for (int r = 0; r < a.R; ++r) a.alpha[r] = alpha[r];
+    DeviceGuard g(recv->device);
+    if (!g.ok) return SYM_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (++recv->epoch == 0) {
+        SYM_CUDA(cudaMemsetAsync(recv->flags, 0, sizeof(uint32_t) * recv->flag_tiles * recv->R, st));
+        recv->epoch = 1;
+    }
+    a.epoch = recv->epoch;
+    a.flags = recv->flags;
+    a.arrivals = recv->arrivals;
+    a.flag_stride = recv->flag_tiles;
+    a.status = recv->ctx->status;
+    a.timeout_ns = default_timeout_ns();
+    const int occ = occupancy((const void*)k_scale_allreduce, kThreads, 0);
+    const size_t cap = (size_t)occ * recv->ctx->num_sms;
+    const size_t per_block = (size_t)a.R * a.R + a.R;
+    const size_t slots = per_block * a.tiles_per_chunk;
+    const size_t grid = std::min(std::max(slots, (size_t)1), cap);
+    a.lag = (uint32_t)ceil_div(grid, per_block) + 1;
+    void* args[] = {&a};
+    // consumers wait on producers of the same launch -> co-residency required
+    SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_scale_allreduce, dim3((unsigned)grid),
+                                         dim3(kThreads), args, 0, st));
+    count_launch();
+    SYM_CUDA(cudaGetLastError());
+    return SYM_OK;
+}

@@ -379,7 +379,8 @@ sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym
         return SYM_ERR_INVALID_ARG;
     const size_t es = dtype_size(dtype);
     if (!es) return SYM_ERR_INVALID_ARG;
-    if (algo != SYM_ALGO_AUTO && algo != SYM_ALGO_COPY && algo != SYM_ALGO_PUT_SIGNAL)
+    if (algo != SYM_ALGO_AUTO && algo != SYM_ALGO_COPY && algo != SYM_ALGO_PUT_SIGNAL &&
+        algo != SYM_ALGO_CE)
         return SYM_ERR_INVALID_ARG;
     const int R = send->R;
     if (sendcount > send->bytes / es) return SYM_ERR_INVALID_ARG;
@@ -389,6 +390,14 @@ sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym
     DeviceGuard g(recv->device);
     if (!g.ok) return SYM_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
+    if (algo == SYM_ALGO_CE) {
+        // destination r receives the R segments back to back: a 2-D copy whose
+        // rows are the senders (source pitch = window stride, dest pitch = S)
+        for (int r = 0; r < R; ++r)
+            SYM_CUDA(cudaMemcpy2DAsync(recv->base + (size_t)r * recv->stride, S, send->base,
+                                       send->stride, S, (size_t)R, cudaMemcpyDeviceToDevice, st));
+        return SYM_OK;
+    }
     if (algo == SYM_ALGO_PUT_SIGNAL) {
         sym_status_t s = launch_put_signal_allgather(send, recv, S, chunk_bytes, chunks_per_signal,
                                                      nullptr, 0, st);

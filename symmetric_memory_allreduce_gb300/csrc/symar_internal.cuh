@@ -58,7 +58,8 @@ struct sym_window {
     uint32_t nsignals, ncounters;
     uint64_t* sig;         // device [R][nsignals]
     uint64_t* cnt;         // device [R][ncounters]
-    uint32_t* flags;       // device [R][flag_tiles]: pull two-shot tile flags
+    uint32_t* flags;       // device [R][flag_tiles]: per-tile ready flags (epoch-tagged)
+    uint32_t* arrivals;    // device [R][flag_tiles]: per-tile producer counters (zero when idle)
     size_t flag_tiles;     // flag slots per rank
     uint32_t epoch;        // last epoch used for the flags (host)
     void* aux;             // the allocation holding sig, cnt and flags

@@ -145,7 +145,7 @@ static sym_status_t alloc_aux(sym_window* w) {
     size_t sig_b = sizeof(uint64_t) * (size_t)w->R * w->nsignals;
     size_t cnt_b = sizeof(uint64_t) * (size_t)w->R * w->ncounters;
     size_t flg_b = sizeof(uint32_t) * (size_t)w->R * w->flag_tiles;
-    size_t total = sig_b + cnt_b + flg_b;
+    size_t total = sig_b + cnt_b + 2 * flg_b;
     char* p = nullptr;
     SYM_CUDA(cudaMalloc(&p, total));
     cudaError_t e = cudaMemset(p, 0, total);
@@ -157,6 +157,7 @@ static sym_status_t alloc_aux(sym_window* w) {
     w->sig = (uint64_t*)p;
     w->cnt = (uint64_t*)(p + sig_b);
     w->flags = (uint32_t*)(p + sig_b + cnt_b);
+    w->arrivals = (uint32_t*)(p + sig_b + cnt_b + flg_b);
     w->epoch = 0;
     return SYM_OK;
 }

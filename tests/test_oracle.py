@@ -468,3 +468,36 @@ def test_alltoall_transpose(oracle, R, B):
     x = rng.integers(0, 256, size=(R, R * B), dtype=np.uint8)
     want = x.reshape(R, R, B).transpose(1, 0, 2).reshape(R, R * B)
     assert np.array_equal(oracle.alltoall(x), want)
+
+
+# ---------------------------------------------------------------- producer + AllReduce
+
+def test_scale_allreduce_reduces_to_allreduce(oracle):
+    rng = np.random.default_rng(41)
+    a = rng.standard_normal((8, 777)).astype(np.float32)
+    s, y = oracle.scale_allreduce(a, np.ones(8))
+    assert np.array_equal(s, a)
+    assert np.array_equal(y.view(np.uint32), oracle.allreduce_sum_f32(a).view(np.uint32))
+
+
+@pytest.mark.parametrize("R", [1, 2, 4, 8, 16])
+def test_scale_allreduce_closed_form(oracle, R):
+    """Rank fill a_r = r with alpha_r = r + 1: y = sum r(r+1) = (R-1)R(R+1)/3 (exact)."""
+    a = np.repeat(np.arange(R, dtype=np.float32)[:, None], 33, axis=1)
+    s, y = oracle.scale_allreduce(a, np.arange(1, R + 1))
+    assert np.all(y == np.float32((R - 1) * R * (R + 1) // 3))
+    assert np.array_equal(s[:, 0], np.arange(R) * np.arange(1, R + 1))
+
+
+def test_scale_allreduce_brute_force(oracle):
+    rng = np.random.default_rng(43)
+    R, n = 5, 64
+    a = rng.standard_normal((R, n)).astype(np.float32)
+    alpha = rng.standard_normal(R).astype(np.float32)
+    s, y = oracle.scale_allreduce(a, alpha)
+    s_ref = np.empty_like(a)
+    for q in range(R):
+        for i in range(n):
+            s_ref[q, i] = np.float32(alpha[q]) * np.float32(a[q, i])
+    assert np.array_equal(s.view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(y.view(np.uint32), _seq_sum_np(s_ref).view(np.uint32))

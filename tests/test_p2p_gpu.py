@@ -31,7 +31,7 @@ def test_allgather_worked_example(symar, oracle):
 
 @pytest.mark.parametrize("R,S", [(1, 48), (3, 4096 + 16), (16, 65536), (5, 1001), (8, 6),
                                  (16, 1 << 20)])
-@pytest.mark.parametrize("algo", ["copy", "put_signal"])
+@pytest.mark.parametrize("algo", ["copy", "put_signal", "ce"])
 def test_allgather_random_bytes(symar, oracle, R, S, algo):
     rng = np.random.default_rng(R * 1000 + S)
     x = rng.integers(0, 256, size=(R, S), dtype=np.uint8)
@@ -44,7 +44,7 @@ def test_allgather_random_bytes(symar, oracle, R, S, algo):
         elif es == 1:
             pytest.skip("a dtype must divide the bytes; odd sizes are covered by put_signal")
         else:
-            symar.sym_allgather(send, recv, S // es, "f32" if es == 4 else "bf16", "copy")
+            symar.sym_allgather(send, recv, S // es, "f32" if es == 4 else "bf16", algo)
         assert symar.sym_stream_status() == symar.SYM_OK
         want = oracle.allgather(x)
         got = download(recv, R * S)
