@@ -197,6 +197,7 @@ struct ArArgs {
     uint32_t lag;            // tile blocks between a reduce and its gathers
     int mode;                // 0 fused, 1 reduce-scatter only, 2 all-gather only
     uint32_t* status;
+    uint32_t tag;            // launch tag for the waits' early give-up
     uint64_t timeout_ns;
 };
 
@@ -362,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_twoshot_bulk(ArArgs a) {
             }
         }
         if (!__syncthreads_and(ok)) {               // uniform: every thread leaves together
-            if (threadIdx.x == 0) report_timeout(a.status, kSiteBulkStage, blockIdx.x, i);
+            if (threadIdx.x == 0) report_timeout(a.status, 0, kSiteBulkStage, blockIdx.x, i);
             break;
         }
         const unsigned char* st = in + (size_t)s * R * tile;
@@ -526,8 +527,8 @@ __global__ void __launch_bounds__(kThreads) k_twoshot_pull(ArArgs a) {
                 const uint32_t* f = a.flags + (size_t)q * a.flag_stride + t;
                 const uint32_t ep = a.epoch;
                 bool got = bounded_spin([&] { return ld_acquire_u32(f) == ep; }, a.timeout_ns,
-                                        a.status);
-                if (!got) report_timeout(a.status, kSitePullFlag, q, t);
+                                        a.status, a.tag);
+                if (!got) report_timeout(a.status, a.tag, kSitePullFlag, q, t);
                 s_ok[parity] = got ? 1 : 0;
             }
             __syncthreads();
@@ -613,6 +614,7 @@ sym_status_t launch_algo(sym_algo_t algo, ArArgs& a, sym_win_t recv, cudaStream_
                 recv->epoch = 1;
             }
             a.epoch = recv->epoch;
+            a.tag = ctx->new_tag();
             a.mode = 0;
             size_t slots = (size_t)a.R * a.R * a.tiles_per_chunk;
             size_t grid = std::min(std::max(slots, (size_t)1), cap);

@@ -28,6 +28,7 @@ struct FusedArgs {
     size_t flag_stride;
     uint32_t epoch, lag;
     uint32_t* status;
+    uint32_t tag;
     uint64_t timeout_ns;
     float alpha[kMaxRanks];
 };
@@ -93,8 +94,8 @@ __global__ void __launch_bounds__(kThreads) k_scale_allreduce(FusedArgs a) {
                 const uint32_t* f = a.flags + (size_t)q * a.flag_stride + t;
                 const uint32_t ep = a.epoch;
                 bool got = bounded_spin([&] { return ld_acquire_u32(f) == ep; }, a.timeout_ns,
-                                        a.status);
-                if (!got) report_timeout(a.status, kSitePullFlag, q, t);
+                                        a.status, a.tag);
+                if (!got) report_timeout(a.status, a.tag, kSitePullFlag, q, t);
                 s_ok[parity] = got ? 1 : 0;
             }
             __syncthreads();
@@ -173,6 +174,7 @@ extern "C" sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_wi
     a.arrivals = recv->arrivals;
     a.flag_stride = recv->flag_tiles;
     a.status = recv->ctx->status;
+    a.tag = recv->ctx->new_tag();
     a.timeout_ns = default_timeout_ns();
     const int occ = occupancy((const void*)k_scale_allreduce, kThreads, 0);
     const size_t cap = (size_t)occ * recv->ctx->num_sms;

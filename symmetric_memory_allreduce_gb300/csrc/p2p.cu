@@ -114,6 +114,7 @@ struct PsArgs {
     uint64_t* mismatch;       // optional prefix-visibility check
     uint32_t nproducers;      // CTAs [0, nproducers) put; the rest only receive
     uint32_t* status;
+    uint32_t tag;
     uint64_t timeout_ns;
     int vec;
 };
@@ -168,8 +169,8 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
             if (threadIdx.x == 0) {
                 const uint64_t want = a.nbatches;
                 if (!bounded_spin([&] { return ld_acquire_u64(sp) >= want; }, a.timeout_ns,
-                                  a.status))
-                    report_timeout(a.status, kSitePutSignalRecv, p, q);
+                                  a.status, a.tag))
+                    report_timeout(a.status, a.tag, kSitePutSignalRecv, p, q);
             }
             continue;
         }
@@ -181,8 +182,8 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
                 uint64_t v = 0;
                 const uint64_t s0 = seen;
                 bool got = bounded_spin([&] { return (v = ld_acquire_u64(sp)) > s0; },
-                                        a.timeout_ns, a.status);
-                if (!got) report_timeout(a.status, kSitePutSignalRecv, p, q);
+                                        a.timeout_ns, a.status, a.tag);
+                if (!got) report_timeout(a.status, a.tag, kSitePutSignalRecv, p, q);
                 s_v[parity] = got ? min(v, (uint64_t)a.nbatches) : ~0ull;
             }
             __syncthreads();
@@ -222,6 +223,7 @@ struct A2aArgs {
     uint32_t nsig;
     uint32_t nproducers;
     uint32_t* status;
+    uint32_t tag;
     uint64_t timeout_ns;
 };
 
@@ -248,8 +250,8 @@ __global__ void __launch_bounds__(kPutThreads) k_alltoall(A2aArgs a) {
         if (threadIdx.x == 0) {
             const uint64_t* sp = a.sig + (size_t)p * a.nsig;
             if (!bounded_spin([&] { return ld_acquire_u64(sp) >= (uint64_t)R; }, a.timeout_ns,
-                              a.status))
-                report_timeout(a.status, kSitePutSignalRecv, p, 0xA2Au);
+                              a.status, a.tag))
+                report_timeout(a.status, a.tag, kSitePutSignalRecv, p, 0xA2Au);
         }
     }
 }
@@ -305,8 +307,8 @@ __global__ void k_wait_slot(const uint64_t* slot, uint64_t least, int bits, uint
                             uint32_t* status, uint32_t site, uint32_t a, uint32_t b) {
     if (threadIdx.x != 0) return;
     bool ok = bounded_spin([&] { return rolling_le_dev(least, ld_acquire_u64(slot), bits); },
-                           timeout_ns, status);
-    if (!ok) report_timeout(status, site, a, b);
+                           timeout_ns, status, 0u);
+    if (!ok) report_timeout(status, 0u, site, a, b);
 }
 
 }  // namespace symar
@@ -343,6 +345,7 @@ static sym_status_t launch_put_signal_allgather(sym_win_t send, sym_win_t recv, 
     a.ncnt = send->ncounters;
     a.mismatch = d_mismatch;
     a.status = recv->ctx->status;
+    a.tag = recv->ctx->new_tag();
     a.timeout_ns = timeout_ns ? timeout_ns : default_timeout_ns();
     if (a.timeout_ns > 60000000000ull) a.timeout_ns = 60000000000ull;
     a.vec = (S % 16 == 0 && chunk % 16 == 0) ? 1 : 0;
@@ -476,6 +479,7 @@ sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtyp
     a.B = count * es;
     a.vec = a.B % 16 == 0 ? 1 : 0;
     a.status = recv->ctx->status;
+    a.tag = recv->ctx->new_tag();
     a.timeout_ns = timeout_ns ? std::min(timeout_ns, (uint64_t)60000000000ull) : default_timeout_ns();
     const size_t pairs = (size_t)R * R;
     const int occ = occupancy((const void*)k_alltoall, kPutThreads, 0);

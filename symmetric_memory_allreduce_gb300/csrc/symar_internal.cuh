@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cuda_bf16.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -34,14 +35,27 @@ enum WaitSite : uint32_t {
 
 // Per-device context: the status block and the arrival ring used by
 // multi-CTA puts to find the last CTA.
+//
+// status[0] bits, [1] site, [2..3] coordinates of the first wait that ran out
+// (read and cleared by sym_stream_status); status[4] = the launch tag of the
+// last launch that gave up.  Every launch that waits gets a fresh tag, so
+// its other waits stop early once one of them has given up, while later
+// launches are not affected by a stale timeout.
 struct DevCtx {
     int device = -1;
     int num_sms = 0;
-    uint32_t* status = nullptr;   // [0] bits, [1] site, [2..3] coordinates
+    uint32_t* status = nullptr;   // kStatusWords words, see above
     uint32_t* arrive = nullptr;   // kArriveRing counters, zero when idle
     uint64_t arrive_next = 0;     // host-side ring cursor
+    std::atomic<uint32_t> next_tag{0};   // host-side launch tags (0 never used)
+    uint32_t new_tag() {
+        uint32_t t = ++next_tag;
+        return t ? t : ++next_tag;
+    }
 };
 constexpr int kArriveRing = 1024;
+constexpr int kStatusWords = 8;
+constexpr int kAbortWord = 4;
 
 DevCtx* dev_ctx(int device);      // created on first use, lives until exit
 
@@ -136,23 +150,25 @@ __device__ __forceinline__ bool rolling_le_dev(uint64_t a, uint64_t b, int bits)
     return d < (1ull << (bits - 1));
 }
 
-// Records a timeout in the device status block (first site wins).
-__device__ __forceinline__ void report_timeout(uint32_t* status, uint32_t site, uint32_t a,
-                                               uint32_t b) {
+// Records a timeout in the device status block (first site wins) and tags
+// the status block with this launch, so the launch's other waits give up.
+__device__ __forceinline__ void report_timeout(uint32_t* status, uint32_t tag, uint32_t site,
+                                               uint32_t a, uint32_t b) {
     uint32_t prev = atomicOr(status, kStatusTimeout);
     if ((prev & kStatusTimeout) == 0) {
         status[1] = site;
         status[2] = a;
         status[3] = b;
     }
+    if (tag) atomicExch(status + kAbortWord, tag);
 }
 
 // Bounded spin: polls pred() with a sleeping back-off until it holds, the
-// timeout elapses, an iteration cap is hit, or another wait of this device
-// has already timed out.  Returns true when pred() held.
+// timeout elapses, an iteration cap is hit, or (tag != 0) another wait of the
+// same launch has already given up.  Returns true when pred() held.
 template <class Pred>
 __device__ __forceinline__ bool bounded_spin(Pred pred, uint64_t timeout_ns,
-                                             const uint32_t* status) {
+                                             const uint32_t* status, uint32_t tag) {
     if (pred()) return true;
     const uint64_t t0 = globaltimer_ns();
     const uint64_t max_iters = timeout_ns / 16u + 65536u;
@@ -162,7 +178,7 @@ __device__ __forceinline__ bool bounded_spin(Pred pred, uint64_t timeout_ns,
         if (sleep_ns < 512) sleep_ns <<= 1;
         if (pred()) return true;
         if ((it & 7u) == 0u) {
-            if (ld_volatile_u32(status) & kStatusTimeout) return false;
+            if (tag && ld_volatile_u32(status + kAbortWord) == tag) return false;
             if (globaltimer_ns() - t0 > timeout_ns) return false;
         }
     }

@@ -119,7 +119,7 @@ DevCtx* dev_ctx(int device) {
     c->device = device;
     if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         c->num_sms = 1;
-    const size_t words = 4 + kArriveRing;
+    const size_t words = kStatusWords + kArriveRing;
     uint32_t* mem = nullptr;
     if (cudaMalloc(&mem, words * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(mem, 0, words * sizeof(uint32_t)) != cudaSuccess) {
@@ -128,7 +128,7 @@ DevCtx* dev_ctx(int device) {
         return nullptr;
     }
     c->status = mem;
-    c->arrive = mem + 4;
+    c->arrive = mem + kStatusWords;
     ctxs[device] = c;
     return c;
 }
