@@ -463,6 +463,130 @@ def run_sweep(args) -> int:
     return 0
 
 
+def _time_launches(fn, iters: int, stream) -> list[float]:
+    """Per-launch CUDA-event times (ms) of fn() on `stream`, after 5 warm-ups."""
+    import torch
+
+    for _ in range(5):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    for s, e in ev:
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in ev]
+
+
+def run_suite(args) -> int:
+    """Every hot-path row on its workload: one JSON object per (row, variant)."""
+    import numpy as np
+    import torch
+
+    import symmetric_memory_allreduce_gb300 as sm
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    torch.cuda.set_device(0)
+    sm.load()
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peak()
+
+    def report(row, variant, ts, per_rank, hbm_bytes, logical_bytes=None, extra=None):
+        med = statistics.median(ts)
+        d = {"row": row, "variant": variant, "iters": len(ts), "us_median": med * 1e3,
+             "us_p10": percentile(ts, 0.1) * 1e3, "us_p90": percentile(ts, 0.9) * 1e3,
+             "algbw_gbs": per_rank / (med * 1e-3) / 1e9,
+             "hbm_model_gbs": hbm_bytes / (med * 1e-3) / 1e9,
+             "frac_of_peak": hbm_bytes / (med * 1e-3) / 1e9 / peak, "peak_gbs": peak,
+             "peak_kind": peak_kind}
+        if logical_bytes:
+            d["logical_gbs"] = logical_bytes / (med * 1e-3) / 1e9
+        if extra:
+            d.update(extra)
+        print(json.dumps(d), flush=True)
+        assert sm.sym_stream_status() == sm.SYM_OK, sm.sym_last_error()
+
+    def iters_for(nbytes):
+        return max(20, min(1000, int(4e9 / max(nbytes, 1))))
+
+    # AllReduce rows: configs 1-3 (fp32, bf16 where stated), every algorithm
+    cases = [(1, "f32", ["oneshot", "twoshot", "twoshot_pull", "twoshot_split"]),
+             (2, "f32", ["oneshot", "twoshot", "twoshot_pull", "twoshot_split"]),
+             (3, "f32", ["twoshot", "twoshot_pull", "twoshot_split"]),
+             (3, "bf16", ["twoshot", "twoshot_pull"])]
+    for cfg, dt, algos in cases:
+        x = wl.config_inputs(cfg)
+        if dt == "bf16":
+            x = wl.to_bf16_bits(x)
+        R, n = x.shape
+        S = n * x.itemsize
+        send, recv = sm.Window(R, S), sm.Window(R, S)
+        for r in range(R):
+            send.write(r, x[r])
+        stream.synchronize()
+        for algo in algos:
+            ts = _time_launches(lambda: sm.sym_allreduce(send, recv, n, dt, "sum", algo),
+                                iters_for(2 * R * S), stream)
+            m = algo_bytes(algo, R, S)
+            report(f"allreduce config{cfg}", f"{algo} {dt}", ts, S, m["compulsory"], m["logical"],
+                   {"R": R, "bytes_per_rank": S, "l2_resident": 2 * R * S < (126 << 20)})
+        send.free()
+        recv.free()
+        del x
+
+    # AllGather (copy, CE) and put+signal AllGather: config 5
+    cfg5 = wl.PUT_SIGNAL
+    R, S = cfg5["R"], cfg5["nbytes"]
+    xb = wl.random_bytes(5, R, S)
+    send, recv = sm.Window(R, S, ncounters=1), sm.Window(R, R * S, nsignals=R)
+    for r in range(R):
+        send.write(r, xb[r])
+    stream.synchronize()
+    comp = R * S + R * R * S
+    for algo in ("copy", "ce"):
+        ts = _time_launches(lambda: sm.sym_allgather(send, recv, S // 4, "f32", algo), 50, stream)
+        report("allgather config5", algo, ts, S, comp, extra={"R": R, "bytes_per_rank": S})
+    for batch in (8, 1, 64):
+        ts = _time_launches(lambda: sm.sym_allgather(send, recv, S // 4, "f32", "put_signal",
+                                                     cfg5["chunk"], batch), 50, stream)
+        report("put_signal allgather config5", f"chunk 64KiB, {batch} chunks/signal", ts, S, comp,
+               extra={"R": R, "bytes_per_rank": S, "signals_per_pair": -(-512 // batch)})
+    send.free()
+    recv.free()
+
+    # AlltoAll: R=8, 32 MiB per rank (R segments of 4 MiB)
+    R, B = 8, 4 << 20
+    xa = wl.random_bytes(6, R, R * B)
+    send, recv = sm.Window(R, R * B), sm.Window(R, R * B, nsignals=1)
+    for r in range(R):
+        send.write(r, xa[r])
+    stream.synchronize()
+    for algo in ("copy", "put_signal"):
+        ts = _time_launches(lambda: sm.sym_alltoall(send, recv, B // 4, "f32", algo), 100, stream)
+        report("alltoall", algo, ts, R * B, 2 * R * R * B, extra={"R": R, "bytes_per_segment": B})
+    send.free()
+    recv.free()
+
+    # fused producer + AllReduce: config-3 size
+    x = wl.config_inputs(3)
+    R, n = x.shape
+    S = n * 4
+    win_in, send, recv = sm.Window(R, S), sm.Window(R, S), sm.Window(R, S)
+    for r in range(R):
+        win_in.write(r, x[r])
+    stream.synchronize()
+    alpha = [1.0 + 0.25 * r for r in range(R)]
+    ts = _time_launches(lambda: sm.sym_scale_allreduce(win_in, send, recv, alpha, n), 100, stream)
+    report("fused producer + allreduce", "scale then two-shot, counter relay", ts, S, 3 * R * S,
+           extra={"R": R, "bytes_per_rank": S, "bytes_model": "read in RS + write contributions RS "
+                                                             "+ write results RS"})
+    for w in (win_in, send, recv):
+        w.free()
+    return 0
+
+
 def parse(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -480,6 +604,8 @@ def parse(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="message-size sweep of every algorithm instead of the contract line")
     ap.add_argument("--sweep-max", type=int, default=1 << 30)
+    ap.add_argument("--suite", action="store_true",
+                    help="time every hot-path row on its workload instead of the contract line")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)          # at least three untimed warm-up steps
     return a
@@ -491,6 +617,8 @@ def main(argv=None) -> int:
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.suite:
+        return run_suite(args)
     return run_ours(args)
 
 
