@@ -143,6 +143,34 @@ sym_status_t sym_window_read(sym_win_t w, int rank, size_t off, void* dst, size_
 sym_status_t sym_allreduce(sym_win_t send, sym_win_t recv, size_t count, sym_dtype_t dtype,
                            sym_op_t op, sym_algo_t algo, sym_stream_t stream);
 
+/* AllReduce that allocates nothing.  The pages have no counterpart: this is
+ * an addition for callers that cannot call cudaMalloc -- engines that reserve
+ * all device memory at start-up and forbid later allocations, plug-ins whose
+ * host framework owns the device allocator, and latency-critical paths that
+ * cannot afford the device-wide synchronisation cudaMalloc / cudaFree may do.
+ * Every other entry point allocates (windows and their slots), so such a
+ * caller passes its own buffers here instead: rank r's input is at
+ * send + r*stride and its result goes to recv + r*stride (device pointers,
+ * 16-byte aligned, stride a multiple of 16 and >= count*sizeof(dtype)); the
+ * R input and R output ranges must not overlap.  The result is the same as
+ * sym_allreduce's (rank-order fold in fp32, one rounding for bf16/fp16; any
+ * op).  The kernel is the fused pull two-shot; its per-tile flags and status
+ * words live in one fixed 256 KiB __device__ array inside this library, which
+ * every GPU that loads the library holds until the process exits.
+ * Limit: R * ceil(ceil(count*sizeof(dtype)/16/R) / 1024) <= 65536 (one flag
+ * per 16 KiB tile of each rank's chunk; about 1 GiB per rank); larger
+ * requests return SYM_ERR_INVALID_ARG with the reason in sym_last_error().
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls on a device share the array and it
+ * keeps the last call's contents (flags carry a per-call epoch, the status
+ * words are cleared at each call), so calls that overlap on the GPU race:
+ * order them on one stream.  If a wait for another block's tile ever runs
+ * out, the waiting block reduces that tile itself from the inputs, so the
+ * result is still complete.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+sym_status_t sym_allreduce_noalloc(const void* send, void* recv, size_t stride, int R, size_t count,
+                                   sym_dtype_t dtype, sym_op_t op, sym_stream_t stream);
+
 /* The algorithm AUTO resolves to for this request (host only, no launch). */
 sym_status_t sym_allreduce_algo(sym_win_t send, size_t count, sym_dtype_t dtype,
                                 sym_algo_t* out);

@@ -9,7 +9,8 @@ from ._binding import (  # noqa: F401
     SymError, Window, header_symbols, load, sym_abi_version, sym_allgather,
     sym_allgather_put_signal, sym_allreduce, sym_alltoall, sym_scale_allreduce, sym_allreduce_algo, sym_counter_read,
     sym_counter_reset, sym_counter_wait, sym_last_error, sym_launch_count, sym_put_signal,
-    sym_signal, sym_signal_read, sym_signal_reset, sym_signal_wait, sym_status_string,
+    sym_allreduce_noalloc, sym_signal, sym_signal_read, sym_signal_reset, sym_signal_wait,
+    sym_status_string,
     sym_stream_status,
 )
 from ._binding import LIB_PATH  # noqa: F401

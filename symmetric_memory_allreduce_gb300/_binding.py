@@ -64,6 +64,7 @@ _SIGS = {
     "sym_put_signal": ([P, P, i32, i32, sz, sz, sz, u32, u32, P], i32),
     "sym_alltoall": ([P, P, sz, i32, i32, u64, P], i32),
     "sym_scale_allreduce": ([P, P, P, P, sz, P], i32),
+    "sym_allreduce_noalloc": ([P, P, sz, i32, sz, i32, i32, P], i32),
     "sym_signal": ([P, i32, u32, u64, P], i32),
     "sym_signal_wait": ([P, i32, u32, u64, i32, u64, P], i32),
     "sym_signal_read": ([P, i32, u32, i32, ctypes.POINTER(u64), P], i32),
@@ -244,6 +245,17 @@ def sym_alltoall(send, recv, count: int, dtype="f32", algo="auto", timeout_ns: i
                  stream=None):
     _check(_lib.sym_alltoall(_handle(send), _handle(recv), count, DTYPES.get(dtype, dtype),
                              ALGOS.get(algo, algo), timeout_ns, _stream(stream)), "sym_alltoall")
+
+
+def sym_allreduce_noalloc(send_ptr: int, recv_ptr: int, stride: int, R: int, count: int,
+                          dtype="f32", op="sum", stream=None):
+    """AllReduce over caller-owned buffers (rank r at ptr + r*stride) that allocates nothing.
+
+    For callers that cannot allocate device memory (e.g. an engine that forbids
+    allocations after start-up, or a plug-in whose framework owns the allocator).
+    """
+    _check(_lib.sym_allreduce_noalloc(send_ptr, recv_ptr, stride, R, count, DTYPES.get(dtype, dtype),
+                                      OPS.get(op, op), _stream(stream)), "sym_allreduce_noalloc")
 
 
 def sym_scale_allreduce(inp, send, recv, alpha, count: int, stream=None):

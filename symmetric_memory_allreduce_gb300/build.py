@@ -19,8 +19,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--fmad=false", "-Xptxas", "-v", "-I", INCLUDE]
-SOURCES = ["window.cu", "allreduce.cu", "allreduce_f32.cu", "allreduce_bf16.cu", "allreduce_f16.cu", "fused.cu",
-           "p2p.cu"]
+SOURCES = ["window.cu", "allreduce.cu", "allreduce_f32.cu", "allreduce_bf16.cu", "allreduce_f16.cu",
+           "fused.cu", "p2p.cu", "noalloc.cu"]
 
 
 def nvcc() -> str:

@@ -85,6 +85,7 @@ namespace symar {
 // ----------------------------------------------------------------- host utils
 
 sym_status_t cuda_fail(cudaError_t e, const char* what);   // records the error text
+void set_last_error(const char* text);                      // text for sym_last_error()
 #define SYM_CUDA(call)                                                   \
     do {                                                                 \
         cudaError_t e_ = (call);                                         \

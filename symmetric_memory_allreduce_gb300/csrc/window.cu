@@ -29,6 +29,10 @@ sym_status_t cuda_fail(cudaError_t e, const char* what) {
     return e == cudaErrorMemoryAllocation ? SYM_ERR_OOM : SYM_ERR_CUDA;
 }
 
+void set_last_error(const char* text) {
+    snprintf(g_last_error, sizeof g_last_error, "%s", text);
+}
+
 DeviceGuard::DeviceGuard(int dev) {
     if (cudaGetDevice(&prev) != cudaSuccess) {
         prev = -1;
