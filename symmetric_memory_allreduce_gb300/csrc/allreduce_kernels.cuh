@@ -430,26 +430,45 @@ __global__ void __launch_bounds__(kThreads) k_oneshot(ArArgs a) {
 
 // ----------------------------------------------------------------- two-shot (pull all-gather)
 
-template <class T, class Op, int RB>
-__device__ __forceinline__ void pull_reduce_item(const ArArgs& a, uint32_t q, uint32_t t) {
-    constexpr int U = kPullU;
-    constexpr size_t TILEV = (size_t)kThreads * U;
+// Reduce tile t of chunk q over all windows and store it into slot `dst_slot`
+// (`keep`: leave it in L2 for the gathers that read it next).  The 16 KiB tile
+// is done in kPullU / 2 sub-steps of two vectors per thread, so that the
+// registers of RB-rank batches stay low enough for three CTAs per SM.
+template <class T, class Op, int RB, bool keep>
+__device__ __forceinline__ void reduce_tile_into(const ArArgs& a, uint32_t q, uint32_t t,
+                                                 uint32_t dst_slot) {
+    constexpr int U = 2;
+    constexpr size_t TILEV = (size_t)kThreads * kPullU;
     const size_t c0 = (size_t)q * a.chunk_vec;
     const size_t c1 = min(c0 + a.chunk_vec, a.nvec);
     const size_t v0 = c0 + (size_t)t * TILEV;
-    size_t idx[U];
-    bool ok[U];
+    char* dst = a.recv + (size_t)dst_slot * a.rstride;
+#pragma unroll 1
+    for (int h = 0; h < kPullU / U; ++h) {
+        size_t idx[U];
+        bool ok[U];
 #pragma unroll
-    for (int k = 0; k < U; ++k) {
-        idx[k] = v0 + threadIdx.x + (size_t)k * kThreads;
-        ok[k] = idx[k] < c1;
+        for (int k = 0; k < U; ++k) {
+            idx[k] = v0 + threadIdx.x + (size_t)(h * U + k) * kThreads;
+            ok[k] = idx[k] < c1;
+        }
+        float acc[U][T::V];
+        reduce_vectors<T, Op, RB, U, keep ? kLoadStream : kLoadKeep>(a.send, a.sstride, a.R, idx,
+                                                                       ok, acc);
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            if (!ok[k]) continue;
+            if (keep)
+                store16_keep(dst + idx[k] * kVecBytes, T::narrow(acc[k]));
+            else
+                store16_stream(dst + idx[k] * kVecBytes, T::narrow(acc[k]));
+        }
     }
-    float acc[U][T::V];
-    reduce_vectors<T, Op, RB, U, kLoadStream>(a.send, a.sstride, a.R, idx, ok, acc);
-    char* dst = a.recv + (size_t)q * a.rstride;
-#pragma unroll
-    for (int k = 0; k < U; ++k)
-        if (ok[k]) store16_keep(dst + idx[k] * kVecBytes, T::narrow(acc[k]));
+}
+
+template <class T, class Op, int RB>
+__device__ __forceinline__ void pull_reduce_item(const ArArgs& a, uint32_t q, uint32_t t) {
+    reduce_tile_into<T, Op, RB, true>(a, q, t, q);
 }
 
 __device__ __forceinline__ void pull_copy_item(const ArArgs& a, uint32_t r, uint32_t q, uint32_t t) {
@@ -473,8 +492,16 @@ __device__ __forceinline__ void pull_copy_item(const ArArgs& a, uint32_t r, uint
     }
 }
 
+// resident CTAs per SM the pull kernels are compiled for (register budget):
+// three for fp32, two for the 16-bit types, whose widened tiles need more
+template <class T>
+constexpr int pull_blocks_per_sm() {
+    return T::V == 4 ? 3 : 2;
+}
+constexpr int kPullBlocksPerSm = 3;
+
 template <class T, class Op, int RB>
-__global__ void __launch_bounds__(kThreads) k_twoshot_pull(ArArgs a) {
+__global__ void __launch_bounds__(kThreads, pull_blocks_per_sm<T>()) k_twoshot_pull(ArArgs a) {
     constexpr size_t TILEV = (size_t)kThreads * kPullU;
     __shared__ int s_ok[2];
     const uint32_t R = (uint32_t)a.R, T_ = a.tiles_per_chunk;
@@ -549,7 +576,7 @@ sym_status_t launch_algo(sym_algo_t algo, ArArgs& a, sym_win_t recv, cudaStream_
     const bool wide = a.R > 4;
     void (*kst)(ArArgs) = wide ? k_twoshot_st<T, Op, 8, 2> : k_twoshot_st<T, Op, 4, 2>;
     void (*kone)(ArArgs) = wide ? k_oneshot<T, Op, 8, 2> : k_oneshot<T, Op, 4, 2>;
-    void (*kpull)(ArArgs) = wide ? k_twoshot_pull<T, Op, 8> : k_twoshot_pull<T, Op, 4>;
+    void (*kpull)(ArArgs) = k_twoshot_pull<T, Op, 4>;   // 4-rank batches: 3 CTAs per SM
     constexpr size_t TILEV2 = (size_t)kThreads * 2, TILEVP = (size_t)kThreads * kPullU;
     a.status = ctx->status;
     a.timeout_ns = default_timeout_ns();

@@ -35,7 +35,7 @@ struct FusedArgs {
 
 // slot sequence in blocks of R*R + R: block b holds the producer items (r, q)
 // of tile b and the consumer items q of tile b - lag.
-__global__ void __launch_bounds__(kThreads) k_scale_allreduce(FusedArgs a) {
+__global__ void __launch_bounds__(kThreads, kPullBlocksPerSm) k_scale_allreduce(FusedArgs a) {
     constexpr int U = kPullU;
     constexpr size_t TILEV = (size_t)kThreads * U;
     __shared__ int s_ok[2];
@@ -102,19 +102,19 @@ __global__ void __launch_bounds__(kThreads) k_scale_allreduce(FusedArgs a) {
             const bool go = s_ok[parity] != 0;
             parity ^= 1u;
             if (!go) continue;
-            float acc[U][4];
-            if (a.R > 4)
-                reduce_vectors<F32T, OpSum, 8, U, kLoadKeep>(a.send, a.sstride, a.R, idx, ok, acc);
-            else
-                reduce_vectors<F32T, OpSum, 4, U, kLoadKeep>(a.send, a.sstride, a.R, idx, ok, acc);
-            uint4 out[U];
-#pragma unroll
-            for (int k = 0; k < U; ++k) out[k] = F32T::narrow(acc[k]);
-            for (int r = 0; r < a.R; ++r) {
-                char* dst = a.recv + (size_t)r * a.rstride;
-#pragma unroll
-                for (int k = 0; k < U; ++k)
-                    if (ok[k]) store16_stream(dst + idx[k] * kVecBytes, out[k]);
+            // two sub-steps of two vectors per thread, ranks folded four at a time
+#pragma unroll 1
+            for (int h = 0; h < U / 2; ++h) {
+                size_t hidx[2] = {idx[2 * h], idx[2 * h + 1]};
+                bool hok[2] = {ok[2 * h], ok[2 * h + 1]};
+                float acc[2][4];
+                reduce_vectors<F32T, OpSum, 4, 2, kLoadKeep>(a.send, a.sstride, a.R, hidx, hok, acc);
+                const uint4 o0 = F32T::narrow(acc[0]), o1 = F32T::narrow(acc[1]);
+                for (int r = 0; r < a.R; ++r) {
+                    char* dst = a.recv + (size_t)r * a.rstride;
+                    if (hok[0]) store16_stream(dst + hidx[0] * kVecBytes, o0);
+                    if (hok[1]) store16_stream(dst + hidx[1] * kVecBytes, o1);
+                }
             }
         }
     }

@@ -43,30 +43,13 @@ static __device__ __align__(256) uint32_t g_static_scratch[kStaticFlagWords + kS
 template <class T, class Op, int RB>
 __device__ __forceinline__ void static_reduce_into(const ArArgs& a, uint32_t r, uint32_t q,
                                                    uint32_t t) {
-    constexpr int U = kPullU;
-    constexpr size_t TILEV = (size_t)kThreads * U;
-    const size_t c0 = (size_t)q * a.chunk_vec;
-    const size_t c1 = min(c0 + a.chunk_vec, a.nvec);
-    const size_t v0 = c0 + (size_t)t * TILEV;
-    size_t idx[U];
-    bool ok[U];
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-        idx[k] = v0 + threadIdx.x + (size_t)k * kThreads;
-        ok[k] = idx[k] < c1;
-    }
-    float acc[U][T::V];
-    reduce_vectors<T, Op, RB, U, kLoadKeep>(a.send, a.sstride, a.R, idx, ok, acc);
-    char* dst = a.recv + (size_t)r * a.rstride;
-#pragma unroll
-    for (int k = 0; k < U; ++k)
-        if (ok[k]) store16_stream(dst + idx[k] * kVecBytes, T::narrow(acc[k]));
+    reduce_tile_into<T, Op, RB, false>(a, q, t, r);
 }
 
 // The fused pull two-shot (see k_twoshot_pull, mode 0) on the static flags.
 template <class T, class Op>
-__global__ void __launch_bounds__(kThreads) k_twoshot_pull_static(ArArgs a) {
-    constexpr int RB = 8;
+__global__ void __launch_bounds__(kThreads, 2) k_twoshot_pull_static(ArArgs a) {
+    constexpr int RB = 4;
     constexpr size_t TILEV = (size_t)kThreads * kPullU;
     __shared__ int s_ok[2];
     const uint32_t R = (uint32_t)a.R, T_ = a.tiles_per_chunk;

@@ -210,17 +210,22 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
 
 // [GIN] pure-GIN AlltoAll: sender q puts segment p of its send buffer into
 // rank p's receive buffer at segment q, with one signal increment per put;
-// the receiver waits for R increments.  Here one CTA moves one (q -> p)
-// segment, then (put+signal form) adds 1 to signal slot 0 of rank p.
+// the receiver waits for R increments.  Here a segment is moved in `pieces`
+// parts by different CTAs (enough parallelism for any R); in the put+signal
+// form the CTA that completes the last part of a (q -> p) segment adds 1 to
+// signal slot 0 of rank p, so each segment put still signals exactly once.
 struct A2aArgs {
     const char* send;
     char* recv;
     size_t sstride, rstride;
     int R;
     size_t B;                 // bytes per segment
+    size_t piece;             // bytes per part (multiple of 16 when vec)
+    uint32_t pieces;          // parts per segment
     int vec;
     uint64_t* sig;            // recv window signals, slot 0 of each rank (put+signal form)
     uint32_t nsig;
+    uint32_t* pair_done;      // [R][R] parts completed, zero when idle (put+signal form)
     uint32_t nproducers;
     uint32_t* status;
     uint32_t tag;
@@ -228,18 +233,25 @@ struct A2aArgs {
 };
 
 __global__ void __launch_bounds__(kPutThreads) k_alltoall(A2aArgs a) {
-    const uint32_t R = (uint32_t)a.R, pairs = R * R;
+    const uint32_t R = (uint32_t)a.R, items = R * R * a.pieces;
     if (blockIdx.x < a.nproducers) {
-        for (uint32_t pr = blockIdx.x; pr < pairs; pr += a.nproducers) {
+        for (uint32_t it = blockIdx.x; it < items; it += a.nproducers) {
+            const uint32_t pr = it / a.pieces, part = it - pr * a.pieces;
             const uint32_t q = pr / R, p = pr - q * R;
             const char* src = a.send + (size_t)q * a.sstride + (size_t)p * a.B;
             char* dst = a.recv + (size_t)p * a.rstride + (size_t)q * a.B;
-            block_copy<kPutThreads, kPutU>(src, dst, 0, a.B, a.vec != 0);
+            const size_t lo = min((size_t)part * a.piece, a.B), hi = min(lo + a.piece, a.B);
+            block_copy<kPutThreads, kPutU>(src, dst, lo, hi, a.vec != 0);
             if (a.sig) {
                 __syncthreads();
                 if (threadIdx.x == 0) {
                     __threadfence();
-                    red_release_add_u64(a.sig + (size_t)p * a.nsig, 1ull);
+                    uint32_t* done = a.pair_done + (size_t)q * R + p;
+                    if (atomicAdd(done, 1u) == a.pieces - 1) {     // last part of the segment
+                        *done = 0;
+                        __threadfence();
+                        red_release_add_u64(a.sig + (size_t)p * a.nsig, 1ull);
+                    }
                 }
             }
         }
@@ -484,18 +496,25 @@ sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtyp
     const size_t pairs = (size_t)R * R;
     const int occ = occupancy((const void*)k_alltoall, kPutThreads, 0);
     const size_t cap = (size_t)occ * recv->ctx->num_sms;
+    // split segments so that about two parts per resident CTA exist, each >= 64 KiB
+    size_t pieces = std::max<size_t>(1, ceil_div(2 * cap, pairs));
+    pieces = std::min(pieces, std::max<size_t>(1, a.B / (64 * 1024)));
+    a.piece = ceil_div(a.B, pieces);
+    if (a.vec) a.piece = ceil_div(a.piece, (size_t)16) * 16;
+    a.pieces = (uint32_t)ceil_div(a.B, a.piece);
+    const size_t items = pairs * a.pieces;
+    a.nproducers = (uint32_t)std::min(items, cap);
     if (signalled) {
         a.sig = recv->sig;
         a.nsig = recv->nsignals;
+        a.pair_done = recv->pair_arrivals;
         k_reset_slot0<<<1, 64, 0, st>>>(a.sig, a.nsig, R);
         count_launch();
-        a.nproducers = (uint32_t)std::min(pairs, cap);
         void* args[] = {&a};
         // receivers wait on senders of the same launch -> co-residency required
         SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_alltoall, dim3(a.nproducers),
                                              dim3(kPutThreads), args, 0, st));
     } else {
-        a.nproducers = (uint32_t)std::min(pairs, cap);
         k_alltoall<<<a.nproducers, kPutThreads, 0, st>>>(a);
     }
     count_launch();

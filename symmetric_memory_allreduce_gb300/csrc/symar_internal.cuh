@@ -74,6 +74,7 @@ struct sym_window {
     uint64_t* cnt;         // device [R][ncounters]
     uint32_t* flags;       // device [R][flag_tiles]: per-tile ready flags (epoch-tagged)
     uint32_t* arrivals;    // device [R][flag_tiles]: per-tile producer counters (zero when idle)
+    uint32_t* pair_arrivals;  // device [R][R]: pieces done per (sender, receiver) (zero when idle)
     size_t flag_tiles;     // flag slots per rank
     uint32_t epoch;        // last epoch used for the flags (host)
     void* aux;             // the allocation holding sig, cnt and flags

@@ -73,7 +73,8 @@ uint64_t default_timeout_ns() {
 }
 
 size_t oneshot_max_bytes() {
-    static const size_t v = (size_t)env_u64("SYM_ONESHOT_MAX_BYTES", 16384);
+    // measured crossover on GB300 (R = 8): one-shot is faster up to 64 KiB per rank
+    static const size_t v = (size_t)env_u64("SYM_ONESHOT_MAX_BYTES", 65536);
     return v;
 }
 
@@ -149,7 +150,8 @@ static sym_status_t alloc_aux(sym_window* w) {
     size_t sig_b = sizeof(uint64_t) * (size_t)w->R * w->nsignals;
     size_t cnt_b = sizeof(uint64_t) * (size_t)w->R * w->ncounters;
     size_t flg_b = sizeof(uint32_t) * (size_t)w->R * w->flag_tiles;
-    size_t total = sig_b + cnt_b + 2 * flg_b;
+    size_t pair_b = sizeof(uint32_t) * (size_t)w->R * w->R;
+    size_t total = sig_b + cnt_b + 2 * flg_b + pair_b;
     char* p = nullptr;
     SYM_CUDA(cudaMalloc(&p, total));
     cudaError_t e = cudaMemset(p, 0, total);
@@ -162,6 +164,7 @@ static sym_status_t alloc_aux(sym_window* w) {
     w->cnt = (uint64_t*)(p + sig_b);
     w->flags = (uint32_t*)(p + sig_b + cnt_b);
     w->arrivals = (uint32_t*)(p + sig_b + cnt_b + flg_b);
+    w->pair_arrivals = (uint32_t*)(p + sig_b + cnt_b + 2 * flg_b);
     w->epoch = 0;
     return SYM_OK;
 }
