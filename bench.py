@@ -349,38 +349,14 @@ def run_ours(args) -> int:
     clk_samples = sampler.window(w0, w1)
     clocks = summarize_clocks(clk_samples, sampler.max_mhz) if clk_samples else nvidia_smi_clocks()
 
-    # e2e: pinned host buffers through the C ABI, copies inside the timed region
+    # e2e: pinned host buffers through the C ABI, copies inside the timed region.
+    # Every step copies its R inputs host -> device (sym_window_write), runs the
+    # AllReduce, and copies all R results device -> host (sym_window_read).  Two
+    # window pairs and three streams let step k+1's inputs cross the host link
+    # while step k's results come back.
     e2e = None
     if not args.no_e2e:
-        e2e_steps = max(3, min(args.steps, args.e2e_steps))
-        h_in = torch.empty((R, S), dtype=torch.uint8, pin_memory=True)
-        h_in.numpy()[:] = x.view(np.uint8)
-        h_out = torch.empty((R, S), dtype=torch.uint8, pin_memory=True)
-        ptr_in, ptr_out = h_in.data_ptr(), h_out.data_ptr()
-
-        def e2e_step():
-            for r in range(R):
-                send.write(r, (ptr_in + r * S, S))
-            step()
-            for r in range(R):
-                recv.read(r, (ptr_out + r * S, S))
-
-        e2e_step()
-        torch.cuda.synchronize()
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
-        e2e = {"value": world * S / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": R * S, "d2h_bytes_per_step": R * S, "steps": e2e_steps,
-               "ms_per_step": e_ms}
-        del h_in, h_out
+        e2e = run_e2e(sm, send, recv, x, R, n, args, world, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -411,6 +387,67 @@ def run_ours(args) -> int:
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def run_e2e(sm, send, recv, x, R, n, args, world, stream) -> dict:
+    """End to end through the C ABI with pinned host buffers (see run_ours)."""
+    import numpy as np
+    import torch
+
+    S = n * 4
+    steps = max(3, min(args.steps, args.e2e_steps))
+    h_in = torch.empty((R, S), dtype=torch.uint8, pin_memory=True)
+    h_in.numpy()[:] = x.view(np.uint8)
+    h_out = [torch.empty((R, S), dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    sends = [send, sm.Window(R, S)]
+    recvs = [recv, sm.Window(R, S)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_done + ev_out:
+        e.record(stream)
+
+    def e2e_step(k):
+        b = k % 2
+        s_in.wait_event(ev_done[b])                 # the AllReduce of step k-2 has read sends[b]
+        for r in range(R):
+            sends[b].write(r, (h_in.data_ptr() + r * S, S), stream=s_in)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])                # the copy-out of step k-2 has read recvs[b]
+        sm.sym_allreduce(sends[b], recvs[b], n, "f32", "sum", args.algo, stream=stream)
+        ev_done[b].record(stream)
+        s_out.wait_event(ev_done[b])
+        for r in range(R):
+            recvs[b].read(r, (h_out[b].data_ptr() + r * S, S), stream=s_out)
+        ev_out[b].record(s_out)
+
+    for k in range(2):                              # warm-up
+        e2e_step(k)
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for k in range(steps):
+        e2e_step(k)
+    stream.wait_event(ev_out[(steps - 1) % 2])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    if sm.sym_stream_status() != sm.SYM_OK:
+        raise RuntimeError("e2e reported a device status: " + sm.sym_last_error())
+    e_ms = max_over_ranks(e0.elapsed_time(e1)) / steps
+    for w in (sends[1], recvs[1]):
+        w.free()
+    return {"value": world * S / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": R * S, "d2h_bytes_per_step": R * S, "steps": steps,
+            "ms_per_step": e_ms,
+            "host_link_gbs": 2 * R * S / (e_ms * 1e-3) / 1e9,
+            "pipeline": "2 window pairs, 3 streams: copy-in || AllReduce || copy-out"}
 
 
 def run_sweep(args) -> int:

@@ -569,6 +569,8 @@ __global__ void __launch_bounds__(kThreads, pull_blocks_per_sm<T>()) k_twoshot_p
 
 // ----------------------------------------------------------------- host launcher
 
+constexpr int kStBlocksPerSm = 1;   // two-shot (store all-gather) launch shape
+
 template <class T, class Op>
 sym_status_t launch_algo(sym_algo_t algo, ArArgs& a, sym_win_t recv, cudaStream_t st) {
     DevCtx* ctx = recv->ctx;
@@ -607,8 +609,11 @@ sym_status_t launch_algo(sym_algo_t algo, ArArgs& a, sym_win_t recv, cudaStream_
             }
             a.tiles_per_chunk = (uint32_t)ceil_div(a.chunk_vec, TILEV2);
             size_t items = (size_t)a.R * a.tiles_per_chunk;
-            int occ = occupancy((const void*)kst, kThreads, 0);
-            size_t grid = std::min(std::max(items, (size_t)1), (size_t)occ * sms);
+            // One resident CTA per SM: 8 warps x 16 loads of 16 B per thread keep
+            // ~64 KB in flight per SM, which measured fastest on GB300 (more in
+            // flight -- two CTAs per SM, 4 vectors per thread, 512 threads --
+            // and less both lost 5-15 % of HBM throughput).
+            size_t grid = std::min(std::max(items, (size_t)1), (size_t)kStBlocksPerSm * sms);
             kst<<<(unsigned)grid, kThreads, 0, st>>>(a);
             count_launch();
             break;
@@ -645,7 +650,7 @@ sym_status_t launch_algo(sym_algo_t algo, ArArgs& a, sym_win_t recv, cudaStream_
             a.mode = 0;
             size_t slots = (size_t)a.R * a.R * a.tiles_per_chunk;
             size_t grid = std::min(std::max(slots, (size_t)1), cap);
-            a.lag = (uint32_t)ceil_div(grid, (size_t)a.R * a.R) + 1;
+            a.lag = (uint32_t)(pull_lag_waves() * ceil_div(grid, (size_t)a.R * a.R)) + 1;
             void* args[] = {&a};
             SYM_CUDA(cudaLaunchCooperativeKernel((const void*)kpull, dim3((unsigned)grid),
                                                  dim3(kThreads), args, 0, st));

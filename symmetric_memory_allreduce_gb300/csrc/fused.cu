@@ -181,7 +181,7 @@ extern "C" sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_wi
     const size_t per_block = (size_t)a.R * a.R + a.R;
     const size_t slots = per_block * a.tiles_per_chunk;
     const size_t grid = std::min(std::max(slots, (size_t)1), cap);
-    a.lag = (uint32_t)ceil_div(grid, per_block) + 1;
+    a.lag = (uint32_t)(pull_lag_waves() * ceil_div(grid, per_block)) + 1;
     void* args[] = {&a};
     // consumers wait on producers of the same launch -> co-residency required
     SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_scale_allreduce, dim3((unsigned)grid),

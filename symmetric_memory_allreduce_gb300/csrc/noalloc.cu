@@ -209,7 +209,7 @@ extern "C" sym_status_t sym_allreduce_noalloc(const void* send, void* recv, size
     a.mode = 0;
     const size_t slots = (size_t)R * R * a.tiles_per_chunk;
     const size_t grid = std::min(std::max(slots, (size_t)1), (size_t)occ * sms);
-    a.lag = (uint32_t)ceil_div(grid, (size_t)R * R) + 1;
+    a.lag = (uint32_t)(pull_lag_waves() * ceil_div(grid, (size_t)R * R)) + 1;
     void* args[] = {&a};
     // gathers wait on reductions of the same launch -> co-residency required
     SYM_CUDA(cudaLaunchCooperativeKernel(kernel, dim3((unsigned)grid), dim3(kThreads), args, 0, st));

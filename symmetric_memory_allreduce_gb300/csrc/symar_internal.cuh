@@ -106,6 +106,9 @@ bool trace_on();
 uint64_t default_timeout_ns();
 size_t oneshot_max_bytes();
 bool twoshot_use_bulk();          // env SYM_TWOSHOT_KERNEL=bulk|ldst
+// Grid waves between a tile's producing item and the items that wait for it
+// (flag-synchronised kernels); env SYM_PULL_LAG_WAVES, default 4, 1..64.
+uint32_t pull_lag_waves();
 int occupancy(const void* kernel, int threads, size_t smem);   // blocks per SM, cached
 size_t dtype_size(sym_dtype_t t);       // 0 if unknown
 

@@ -78,6 +78,14 @@ size_t oneshot_max_bytes() {
     return v;
 }
 
+uint32_t pull_lag_waves() {
+    static const uint32_t v = [] {
+        uint64_t w = env_u64("SYM_PULL_LAG_WAVES", 8);
+        return (uint32_t)(w < 1 ? 1 : (w > 64 ? 64 : w));
+    }();
+    return v;
+}
+
 bool twoshot_use_bulk() {
     static const bool v = [] {
         const char* s = getenv("SYM_TWOSHOT_KERNEL");
