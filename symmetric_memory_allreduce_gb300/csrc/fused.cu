@@ -33,11 +33,16 @@ struct FusedArgs {
     float alpha[kMaxRanks];
 };
 
+// The relay tile: 64 KiB of a chunk (16 vectors per thread in flight for a
+// producer item); the window's flag slots, sized for 16 KiB tiles, suffice.
+constexpr int kFusedU = 16;
+constexpr size_t kFusedTileV = (size_t)kThreads * kFusedU;
+
 // slot sequence in blocks of R*R + R: block b holds the producer items (r, q)
 // of tile b and the consumer items q of tile b - lag.
-__global__ void __launch_bounds__(kThreads, kPullBlocksPerSm) k_scale_allreduce(FusedArgs a) {
-    constexpr int U = kPullU;
-    constexpr size_t TILEV = (size_t)kThreads * U;
+__global__ void __launch_bounds__(kThreads, 2) k_scale_allreduce(FusedArgs a) {
+    constexpr int U = kFusedU;
+    constexpr size_t TILEV = kFusedTileV;
     __shared__ int s_ok[2];
     const uint32_t R = (uint32_t)a.R, T_ = a.tiles_per_chunk;
     const uint32_t per_block = R * R + R;
@@ -54,30 +59,27 @@ __global__ void __launch_bounds__(kThreads, kPullBlocksPerSm) k_scale_allreduce(
         const size_t c1 = min(c0 + a.chunk_vec, a.nvec);
         const size_t v0 = c0 + (size_t)t * TILEV;
         if (v0 >= c1) continue;
-        size_t idx[U];
-        bool ok[U];
-#pragma unroll
-        for (int k = 0; k < U; ++k) {
-            idx[k] = v0 + threadIdx.x + (size_t)k * kThreads;
-            ok[k] = idx[k] < c1;
-        }
+        const size_t base = v0 + threadIdx.x;          // this thread's k-th vector: base + k*kThreads
         if (producer) {
             const uint32_t r = s / R;
             const float al = a.alpha[r];
-            const char* src = a.in + (size_t)r * a.istride;
-            char* dst = a.send + (size_t)r * a.sstride;
+            const uint4* src = reinterpret_cast<const uint4*>(a.in + (size_t)r * a.istride);
+            uint4* dst = reinterpret_cast<uint4*>(a.send + (size_t)r * a.sstride);
             uint4 v[U];
 #pragma unroll
-            for (int k = 0; k < U; ++k)
-                if (ok[k]) v[k] = __ldcs(reinterpret_cast<const uint4*>(src + idx[k] * kVecBytes));
+            for (int k = 0; k < U; ++k) {
+                const size_t i = base + (size_t)k * kThreads;
+                if (i < c1) v[k] = __ldcs(src + i);
+            }
 #pragma unroll
             for (int k = 0; k < U; ++k) {
-                if (!ok[k]) continue;
+                const size_t i = base + (size_t)k * kThreads;
+                if (i >= c1) continue;
                 float f[4];
                 F32T::widen(v[k], f);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) f[e] = __fmul_rn(al, f[e]);
-                store16_keep(dst + idx[k] * kVecBytes, F32T::narrow(f));
+                __stcg(dst + i, F32T::narrow(f));
             }
             __syncthreads();
             if (threadIdx.x == 0) {
@@ -102,11 +104,12 @@ __global__ void __launch_bounds__(kThreads, kPullBlocksPerSm) k_scale_allreduce(
             const bool go = s_ok[parity] != 0;
             parity ^= 1u;
             if (!go) continue;
-            // two sub-steps of two vectors per thread, ranks folded four at a time
+            // sub-steps of two vectors per thread, ranks folded four at a time
 #pragma unroll 1
             for (int h = 0; h < U / 2; ++h) {
-                size_t hidx[2] = {idx[2 * h], idx[2 * h + 1]};
-                bool hok[2] = {ok[2 * h], ok[2 * h + 1]};
+                const size_t hidx[2] = {base + (size_t)(2 * h) * kThreads,
+                                        base + (size_t)(2 * h + 1) * kThreads};
+                const bool hok[2] = {hidx[0] < c1, hidx[1] < c1};
                 float acc[2][4];
                 reduce_vectors<F32T, OpSum, 4, 2, kLoadKeep>(a.send, a.sstride, a.R, hidx, hok, acc);
                 const uint4 o0 = F32T::narrow(acc[0]), o1 = F32T::narrow(acc[1]);
@@ -159,7 +162,7 @@ extern "C" sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_wi
     a.chunk_vec = ceil_div(a.nvec, (size_t)a.R);
     a.tail_elem0 = a.nvec * 4;
     a.tail_n = (uint32_t)(count - a.tail_elem0);
-    a.tiles_per_chunk = (uint32_t)ceil_div(a.chunk_vec, (size_t)kThreads * kPullU);
+    a.tiles_per_chunk = (uint32_t)ceil_div(a.chunk_vec, kFusedTileV);
     if (a.tiles_per_chunk > recv->flag_tiles) return SYM_ERR_INVALID_ARG;
     for (int r = 0; r < a.R; ++r) a.alpha[r] = alpha[r];
     DeviceGuard g(recv->device);
