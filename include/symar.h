@@ -137,7 +137,11 @@ sym_status_t sym_window_read(sym_win_t w, int rank, size_t off, void* dst, size_
  * count: elements per rank; count*sizeof(dtype) <= bytes of both windows.
  * send == recv (in place) is allowed for the two-shot algorithms, not for
  * ONESHOT.  count == 0 is a no-op.  AUTO picks ONESHOT up to
- * SYM_ONESHOT_MAX_BYTES per rank (env), else TWOSHOT.
+ * SYM_ONESHOT_MAX_BYTES per rank (env, default 64 KiB), else TWOSHOT.
+ * TWOSHOT_PULL enqueues a one-thread kernel that advances the recv window's
+ * flag epoch on the device before the main launch, so the call can be
+ * recorded into a CUDA graph and replayed; every algorithm only enqueues
+ * kernels (no host synchronisation) after its first call on a device.
  * Errors: INVALID_ARG (windows of different R or device, count too large,
  * bad algo), UNSUPPORTED (op/dtype/in-place combination), CUDA. */
 sym_status_t sym_allreduce(sym_win_t send, sym_win_t recv, size_t count, sym_dtype_t dtype,
@@ -207,6 +211,11 @@ sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym
  * prefix visibility while they wait: each time a signal grows from a to b
  * they compare batches a..b-1 with the source and add differing bytes to
  * *d_mismatch (expected 0).  Requires recv nsignals >= R, send ncounters >= 1.
+ * If one receiver's wait runs out, the launch's other waits stop early (each
+ * launch is tagged with the recv window's device epoch).  For failure tests,
+ * env SYM_TEST_DROP_LAST_SIGNAL=1 makes the (0 -> 0) stream omit its last
+ * signal, so that receiver's wait runs out (read once per process; off by
+ * default).
  * Errors: INVALID_ARG, CUDA; a wait that runs out -> SYM_ERR_TIMEOUT from
  * sym_stream_status(). */
 sym_status_t sym_allgather_put_signal(sym_win_t send, sym_win_t recv, size_t bytes_per_rank,

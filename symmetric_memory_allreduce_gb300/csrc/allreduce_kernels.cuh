@@ -41,6 +41,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <type_traits>
 
 #include "symar_internal.cuh"
 
@@ -193,11 +194,13 @@ struct ArArgs {
     // pull two-shot
     uint32_t* flags;
     size_t flag_stride;
-    uint32_t epoch;
+    uint32_t epoch;          // flag epoch given by the host (static-scratch variant)
+    const uint32_t* epoch_ptr;   // device epoch word of the window (window variants)
     uint32_t lag;            // tile blocks between a reduce and its gathers
     int mode;                // 0 fused, 1 reduce-scatter only, 2 all-gather only
     uint32_t* status;
-    uint32_t tag;            // launch tag for the waits' early give-up
+    uint32_t* giveup;        // give-up word of the waits (see report_timeout)
+    uint32_t tag;            // this launch's give-up tag (static-scratch variant)
     uint64_t timeout_ns;
 };
 
@@ -363,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_twoshot_bulk(ArArgs a) {
             }
         }
         if (!__syncthreads_and(ok)) {               // uniform: every thread leaves together
-            if (threadIdx.x == 0) report_timeout(a.status, 0, kSiteBulkStage, blockIdx.x, i);
+            if (threadIdx.x == 0) report_timeout(a.status, nullptr, 0, kSiteBulkStage, blockIdx.x, i);
             break;
         }
         const unsigned char* st = in + (size_t)s * R * tile;
@@ -493,15 +496,16 @@ __device__ __forceinline__ void pull_copy_item(const ArArgs& a, uint32_t r, uint
 }
 
 // resident CTAs per SM the pull kernels are compiled for (register budget):
-// three for fp32, two for the 16-bit types, whose widened tiles need more
-template <class T>
+// three, except two for max/min on the 16-bit types, whose widened tiles and
+// compare chains would otherwise spill
+template <class T, class Op>
 constexpr int pull_blocks_per_sm() {
-    return T::V == 4 ? 3 : 2;
+    return (T::V == 8 && !std::is_same<Op, OpSum>::value) ? 2 : 3;
 }
 constexpr int kPullBlocksPerSm = 3;
 
 template <class T, class Op, int RB>
-__global__ void __launch_bounds__(kThreads, pull_blocks_per_sm<T>()) k_twoshot_pull(ArArgs a) {
+__global__ void __launch_bounds__(kThreads, pull_blocks_per_sm<T, Op>()) k_twoshot_pull(ArArgs a) {
     constexpr size_t TILEV = (size_t)kThreads * kPullU;
     __shared__ int s_ok[2];
     const uint32_t R = (uint32_t)a.R, T_ = a.tiles_per_chunk;
@@ -531,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, pull_blocks_per_sm<T>()) k_twoshot_p
     }
     // fused: slot sequence in blocks of R*R; block b holds the reduce items of
     // tile b and the gather items of tile b - lag.
+    const uint32_t ep = read_epoch(a.epoch_ptr);
     const uint64_t total = (uint64_t)(T_ + a.lag) * RR;
     for (uint64_t w = blockIdx.x; w < total; w += gridDim.x) {
         const uint32_t b = (uint32_t)(w / RR), s = (uint32_t)(w - (uint64_t)b * RR);
@@ -541,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, pull_blocks_per_sm<T>()) k_twoshot_p
             __syncthreads();
             if (threadIdx.x == 0) {
                 __threadfence();
-                st_release_u32(a.flags + (size_t)q * a.flag_stride + t, a.epoch);
+                st_release_u32(a.flags + (size_t)q * a.flag_stride + t, ep);
             }
         } else {
             if (b < a.lag) continue;
@@ -552,10 +557,9 @@ __global__ void __launch_bounds__(kThreads, pull_blocks_per_sm<T>()) k_twoshot_p
             if (!tile_nonempty(q, t)) continue;
             if (threadIdx.x == 0) {
                 const uint32_t* f = a.flags + (size_t)q * a.flag_stride + t;
-                const uint32_t ep = a.epoch;
                 bool got = bounded_spin([&] { return ld_acquire_u32(f) == ep; }, a.timeout_ns,
-                                        a.status, a.tag);
-                if (!got) report_timeout(a.status, a.tag, kSitePullFlag, q, t);
+                                        a.giveup, ep);
+                if (!got) report_timeout(a.status, a.giveup, ep, kSitePullFlag, q, t);
                 s_ok[parity] = got ? 1 : 0;
             }
             __syncthreads();
@@ -640,13 +644,12 @@ sym_status_t launch_algo(sym_algo_t algo, ArArgs& a, sym_win_t recv, cudaStream_
                 break;
             }
             // fused: blocks wait on one another -> co-residency via a cooperative launch
-            if (++recv->epoch == 0) {
-                SYM_CUDA(cudaMemsetAsync(recv->flags, 0,
-                                         sizeof(uint32_t) * recv->flag_tiles * recv->R, st));
-                recv->epoch = 1;
+            {
+                sym_status_t s = bump_epoch(recv->epoch, st);
+                if (s != SYM_OK) return s;
             }
-            a.epoch = recv->epoch;
-            a.tag = ctx->new_tag();
+            a.epoch_ptr = recv->epoch;
+            a.giveup = recv->giveup;
             a.mode = 0;
             size_t slots = (size_t)a.R * a.R * a.tiles_per_chunk;
             size_t grid = std::min(std::max(slots, (size_t)1), cap);

@@ -26,9 +26,10 @@ struct FusedArgs {
     uint32_t* flags;
     uint32_t* arrivals;
     size_t flag_stride;
-    uint32_t epoch, lag;
+    const uint32_t* epoch;   // device epoch word of the recv window
+    uint32_t lag;
     uint32_t* status;
-    uint32_t tag;
+    uint32_t* giveup;        // the recv window's give-up word
     uint64_t timeout_ns;
     float alpha[kMaxRanks];
 };
@@ -44,6 +45,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_scale_allreduce(FusedArgs a) {
     constexpr int U = kFusedU;
     constexpr size_t TILEV = kFusedTileV;
     __shared__ int s_ok[2];
+    const uint32_t ep = read_epoch(a.epoch);
     const uint32_t R = (uint32_t)a.R, T_ = a.tiles_per_chunk;
     const uint32_t per_block = R * R + R;
     uint32_t parity = 0;
@@ -88,16 +90,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_scale_allreduce(FusedArgs a) {
                 if (atomicAdd(cnt, 1u) == R - 1) {          // the last of the R producers
                     *cnt = 0;
                     __threadfence();
-                    st_release_u32(a.flags + (size_t)q * a.flag_stride + t, a.epoch);
+                    st_release_u32(a.flags + (size_t)q * a.flag_stride + t, ep);
                 }
             }
         } else {
             if (threadIdx.x == 0) {
                 const uint32_t* f = a.flags + (size_t)q * a.flag_stride + t;
-                const uint32_t ep = a.epoch;
                 bool got = bounded_spin([&] { return ld_acquire_u32(f) == ep; }, a.timeout_ns,
-                                        a.status, a.tag);
-                if (!got) report_timeout(a.status, a.tag, kSitePullFlag, q, t);
+                                        a.giveup, ep);
+                if (!got) report_timeout(a.status, a.giveup, ep, kSitePullFlag, q, t);
                 s_ok[parity] = got ? 1 : 0;
             }
             __syncthreads();
@@ -168,16 +169,16 @@ extern "C" sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_wi
     DeviceGuard g(recv->device);
     if (!g.ok) return SYM_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
-    if (++recv->epoch == 0) {
-        SYM_CUDA(cudaMemsetAsync(recv->flags, 0, sizeof(uint32_t) * recv->flag_tiles * recv->R, st));
-        recv->epoch = 1;
+    {
+        sym_status_t s = bump_epoch(recv->epoch, st);
+        if (s != SYM_OK) return s;
     }
     a.epoch = recv->epoch;
     a.flags = recv->flags;
     a.arrivals = recv->arrivals;
     a.flag_stride = recv->flag_tiles;
     a.status = recv->ctx->status;
-    a.tag = recv->ctx->new_tag();
+    a.giveup = recv->giveup;
     a.timeout_ns = default_timeout_ns();
     const int occ = occupancy((const void*)k_scale_allreduce, kThreads, 0);
     const size_t cap = (size_t)occ * recv->ctx->num_sms;

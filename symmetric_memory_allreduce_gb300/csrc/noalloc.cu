@@ -82,8 +82,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_twoshot_pull_static(ArArgs a) {
                 const uint32_t* f = a.flags + (size_t)q * a.flag_stride + t;
                 const uint32_t ep = a.epoch;
                 bool got = bounded_spin([&] { return ld_acquire_u32(f) == ep; }, a.timeout_ns,
-                                        a.status, a.tag);
-                if (!got) report_timeout(a.status, a.tag, kSitePullFlag, q, t);
+                                        a.giveup, a.tag);
+                if (!got) report_timeout(a.status, a.giveup, a.tag, kSitePullFlag, q, t);
                 s_ok[parity] = got ? 1 : 0;
             }
             __syncthreads();
@@ -205,6 +205,7 @@ extern "C" sym_status_t sym_allreduce_noalloc(const void* send, void* recv, size
     a.flags = scratch;
     a.flag_stride = a.tiles_per_chunk;
     a.status = scratch + kStaticFlagWords;
+    a.giveup = scratch + kStaticFlagWords + 4;
     a.timeout_ns = default_timeout_ns();
     a.mode = 0;
     const size_t slots = (size_t)R * R * a.tiles_per_chunk;

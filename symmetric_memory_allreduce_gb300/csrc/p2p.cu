@@ -114,9 +114,11 @@ struct PsArgs {
     uint64_t* mismatch;       // optional prefix-visibility check
     uint32_t nproducers;      // CTAs [0, nproducers) put; the rest only receive
     uint32_t* status;
-    uint32_t tag;
+    const uint32_t* epoch;    // recv window epoch (this launch's give-up tag)
+    uint32_t* giveup;         // recv window give-up word
     uint64_t timeout_ns;
     int vec;
+    int drop_last_signal;     // fault injection for tests: pair (0 -> 0) omits its last signal
 };
 
 __device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* s_red) {
@@ -135,6 +137,7 @@ __device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* s_red) {
 __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) {
     __shared__ uint64_t s_v[2];
     __shared__ uint64_t s_red[kPutThreads / 32];
+    const uint32_t tag = read_epoch(a.epoch);      // bumped by the reset kernel before
     const uint32_t R = (uint32_t)a.R, pairs = R * R;
     // ---- senders: one CTA streams all batches of a (q -> p) pair in order
     if (blockIdx.x < a.nproducers) {
@@ -151,7 +154,8 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
                     __threadfence();
                     atomicAdd(reinterpret_cast<unsigned long long*>(a.cnt + (size_t)q * a.ncnt),
                               (unsigned long long)(k1 - k0));          // local completion
-                    red_release_add_u64(a.sig + (size_t)p * a.nsig + q, 1ull);   // strong signal
+                    const bool dropped = a.drop_last_signal && pr == 0 && b + 1 == a.nbatches;
+                    if (!dropped) red_release_add_u64(a.sig + (size_t)p * a.nsig + q, 1ull);
                 }
             }
         }
@@ -169,8 +173,8 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
             if (threadIdx.x == 0) {
                 const uint64_t want = a.nbatches;
                 if (!bounded_spin([&] { return ld_acquire_u64(sp) >= want; }, a.timeout_ns,
-                                  a.status, a.tag))
-                    report_timeout(a.status, a.tag, kSitePutSignalRecv, p, q);
+                                  a.giveup, tag))
+                    report_timeout(a.status, a.giveup, tag, kSitePutSignalRecv, p, q);
             }
             continue;
         }
@@ -182,8 +186,8 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
                 uint64_t v = 0;
                 const uint64_t s0 = seen;
                 bool got = bounded_spin([&] { return (v = ld_acquire_u64(sp)) > s0; },
-                                        a.timeout_ns, a.status, a.tag);
-                if (!got) report_timeout(a.status, a.tag, kSitePutSignalRecv, p, q);
+                                        a.timeout_ns, a.giveup, tag);
+                if (!got) report_timeout(a.status, a.giveup, tag, kSitePutSignalRecv, p, q);
                 s_v[parity] = got ? min(v, (uint64_t)a.nbatches) : ~0ull;
             }
             __syncthreads();
@@ -228,11 +232,13 @@ struct A2aArgs {
     uint32_t* pair_done;      // [R][R] parts completed, zero when idle (put+signal form)
     uint32_t nproducers;
     uint32_t* status;
-    uint32_t tag;
+    const uint32_t* epoch;    // recv window epoch (put+signal form: the give-up tag)
+    uint32_t* giveup;         // recv window give-up word
     uint64_t timeout_ns;
 };
 
 __global__ void __launch_bounds__(kPutThreads) k_alltoall(A2aArgs a) {
+    const uint32_t tag = a.sig ? read_epoch(a.epoch) : 0u;   // uniform: a.sig is per launch
     const uint32_t R = (uint32_t)a.R, items = R * R * a.pieces;
     if (blockIdx.x < a.nproducers) {
         for (uint32_t it = blockIdx.x; it < items; it += a.nproducers) {
@@ -262,22 +268,34 @@ __global__ void __launch_bounds__(kPutThreads) k_alltoall(A2aArgs a) {
         if (threadIdx.x == 0) {
             const uint64_t* sp = a.sig + (size_t)p * a.nsig;
             if (!bounded_spin([&] { return ld_acquire_u64(sp) >= (uint64_t)R; }, a.timeout_ns,
-                              a.status, a.tag))
-                report_timeout(a.status, a.tag, kSitePutSignalRecv, p, 0xA2Au);
+                              a.giveup, tag))
+                report_timeout(a.status, a.giveup, tag, kSitePutSignalRecv, p, 0xA2Au);
         }
     }
 }
 
-__global__ void k_reset_slot0(uint64_t* sig, uint32_t nsig, int R) {
-    for (int p = threadIdx.x; p < R; p += blockDim.x) sig[(size_t)p * nsig] = 0;
+// The reset kernels run in stream order before the launch that waits; they
+// also advance the receiving window's epoch, the waiting launch's give-up tag.
+__device__ __forceinline__ void bump_epoch_here(uint32_t* epoch) {
+    if (threadIdx.x == 0) {
+        const uint32_t e = *epoch + 1u;
+        *epoch = e ? e : 1u;
+    }
 }
 
-__global__ void k_reset_slots(uint64_t* sig, uint32_t nsig, uint64_t* cnt, uint32_t ncnt, int R) {
+__global__ void k_reset_slot0(uint64_t* sig, uint32_t nsig, int R, uint32_t* epoch) {
+    for (int p = threadIdx.x; p < R; p += blockDim.x) sig[(size_t)p * nsig] = 0;
+    bump_epoch_here(epoch);
+}
+
+__global__ void k_reset_slots(uint64_t* sig, uint32_t nsig, uint64_t* cnt, uint32_t ncnt, int R,
+                              uint32_t* epoch) {
     for (int i = threadIdx.x; i < R * R; i += blockDim.x) {
         const int p = i / R, q = i - p * R;
         sig[(size_t)p * nsig + q] = 0;
     }
     for (int q = threadIdx.x; q < R; q += blockDim.x) cnt[(size_t)q * ncnt] = 0;
+    bump_epoch_here(epoch);
 }
 
 // ----------------------------------------------------------------- single put
@@ -319,8 +337,8 @@ __global__ void k_wait_slot(const uint64_t* slot, uint64_t least, int bits, uint
                             uint32_t* status, uint32_t site, uint32_t a, uint32_t b) {
     if (threadIdx.x != 0) return;
     bool ok = bounded_spin([&] { return rolling_le_dev(least, ld_acquire_u64(slot), bits); },
-                           timeout_ns, status, 0u);
-    if (!ok) report_timeout(status, 0u, site, a, b);
+                           timeout_ns, nullptr, 0u);
+    if (!ok) report_timeout(status, nullptr, 0u, site, a, b);
 }
 
 }  // namespace symar
@@ -357,11 +375,13 @@ static sym_status_t launch_put_signal_allgather(sym_win_t send, sym_win_t recv, 
     a.ncnt = send->ncounters;
     a.mismatch = d_mismatch;
     a.status = recv->ctx->status;
-    a.tag = recv->ctx->new_tag();
+    a.epoch = recv->epoch;
+    a.giveup = recv->giveup;
     a.timeout_ns = timeout_ns ? timeout_ns : default_timeout_ns();
     if (a.timeout_ns > 60000000000ull) a.timeout_ns = 60000000000ull;
     a.vec = (S % 16 == 0 && chunk % 16 == 0) ? 1 : 0;
-    k_reset_slots<<<1, 256, 0, st>>>(a.sig, a.nsig, a.cnt, a.ncnt, R);
+    a.drop_last_signal = test_drop_last_signal() ? 1 : 0;
+    k_reset_slots<<<1, 256, 0, st>>>(a.sig, a.nsig, a.cnt, a.ncnt, R, recv->epoch);
     count_launch();
     const int occ = occupancy((const void*)k_put_signal_allgather, kPutThreads, 0);
     const size_t cap = (size_t)occ * recv->ctx->num_sms;
@@ -491,7 +511,8 @@ sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtyp
     a.B = count * es;
     a.vec = a.B % 16 == 0 ? 1 : 0;
     a.status = recv->ctx->status;
-    a.tag = recv->ctx->new_tag();
+    a.epoch = recv->epoch;
+    a.giveup = recv->giveup;
     a.timeout_ns = timeout_ns ? std::min(timeout_ns, (uint64_t)60000000000ull) : default_timeout_ns();
     const size_t pairs = (size_t)R * R;
     const int occ = occupancy((const void*)k_alltoall, kPutThreads, 0);
@@ -508,7 +529,7 @@ sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtyp
         a.sig = recv->sig;
         a.nsig = recv->nsignals;
         a.pair_done = recv->pair_arrivals;
-        k_reset_slot0<<<1, 64, 0, st>>>(a.sig, a.nsig, R);
+        k_reset_slot0<<<1, 64, 0, st>>>(a.sig, a.nsig, R, recv->epoch);
         count_launch();
         void* args[] = {&a};
         // receivers wait on senders of the same launch -> co-residency required

@@ -37,25 +37,17 @@ enum WaitSite : uint32_t {
 // multi-CTA puts to find the last CTA.
 //
 // status[0] bits, [1] site, [2..3] coordinates of the first wait that ran out
-// (read and cleared by sym_stream_status); status[4] = the launch tag of the
-// last launch that gave up.  Every launch that waits gets a fresh tag, so
-// its other waits stop early once one of them has given up, while later
-// launches are not affected by a stale timeout.
+// (read and cleared by sym_stream_status).  A launch's other waits stop early
+// through the give-up word of its window (see report_timeout).
 struct DevCtx {
     int device = -1;
     int num_sms = 0;
     uint32_t* status = nullptr;   // kStatusWords words, see above
     uint32_t* arrive = nullptr;   // kArriveRing counters, zero when idle
     uint64_t arrive_next = 0;     // host-side ring cursor
-    std::atomic<uint32_t> next_tag{0};   // host-side launch tags (0 never used)
-    uint32_t new_tag() {
-        uint32_t t = ++next_tag;
-        return t ? t : ++next_tag;
-    }
 };
 constexpr int kArriveRing = 1024;
 constexpr int kStatusWords = 8;
-constexpr int kAbortWord = 4;
 
 DevCtx* dev_ctx(int device);      // created on first use, lives until exit
 
@@ -76,7 +68,8 @@ struct sym_window {
     uint32_t* arrivals;    // device [R][flag_tiles]: per-tile producer counters (zero when idle)
     uint32_t* pair_arrivals;  // device [R][R]: pieces done per (sender, receiver) (zero when idle)
     size_t flag_tiles;     // flag slots per rank
-    uint32_t epoch;        // last epoch used for the flags (host)
+    uint32_t* epoch;       // device word: epoch of the last waiting launch (bumped on device)
+    uint32_t* giveup;      // device word: epoch of the last launch whose wait gave up
     void* aux;             // the allocation holding sig, cnt and flags
     symar::DevCtx* ctx;
 };
@@ -109,6 +102,10 @@ bool twoshot_use_bulk();          // env SYM_TWOSHOT_KERNEL=bulk|ldst
 // Grid waves between a tile's producing item and the items that wait for it
 // (flag-synchronised kernels); env SYM_PULL_LAG_WAVES, default 4, 1..64.
 uint32_t pull_lag_waves();
+// Fault injection for failure-detection tests (env SYM_TEST_DROP_LAST_SIGNAL=1):
+// the put + signal AllGather's (0 -> 0) stream omits its last signal, so its
+// receiver's bounded wait runs out.  Off by default; never needs a GPU fault.
+bool test_drop_last_signal();
 int occupancy(const void* kernel, int threads, size_t smem);   // blocks per SM, cached
 size_t dtype_size(sym_dtype_t t);       // 0 if unknown
 
@@ -155,25 +152,28 @@ __device__ __forceinline__ bool rolling_le_dev(uint64_t a, uint64_t b, int bits)
     return d < (1ull << (bits - 1));
 }
 
-// Records a timeout in the device status block (first site wins) and tags
-// the status block with this launch, so the launch's other waits give up.
-__device__ __forceinline__ void report_timeout(uint32_t* status, uint32_t tag, uint32_t site,
-                                               uint32_t a, uint32_t b) {
+// Records a timeout in the device status block (first site wins) and writes
+// this launch's tag into its give-up word, so the launch's other waits stop.
+// The give-up word belongs to the window the launch works on (calls on one
+// window never overlap), and the tag is the window's device epoch of that
+// launch, so a stale give-up never matches a later launch or a graph replay.
+__device__ __forceinline__ void report_timeout(uint32_t* status, uint32_t* giveup, uint32_t tag,
+                                               uint32_t site, uint32_t a, uint32_t b) {
     uint32_t prev = atomicOr(status, kStatusTimeout);
     if ((prev & kStatusTimeout) == 0) {
         status[1] = site;
         status[2] = a;
         status[3] = b;
     }
-    if (tag) atomicExch(status + kAbortWord, tag);
+    if (giveup && tag) atomicExch(giveup, tag);
 }
 
 // Bounded spin: polls pred() with a sleeping back-off until it holds, the
-// timeout elapses, an iteration cap is hit, or (tag != 0) another wait of the
-// same launch has already given up.  Returns true when pred() held.
+// timeout elapses, an iteration cap is hit, or (giveup != null) another wait
+// of the same launch has already given up.  Returns true when pred() held.
 template <class Pred>
 __device__ __forceinline__ bool bounded_spin(Pred pred, uint64_t timeout_ns,
-                                             const uint32_t* status, uint32_t tag) {
+                                             const uint32_t* giveup, uint32_t tag) {
     if (pred()) return true;
     const uint64_t t0 = globaltimer_ns();
     const uint64_t max_iters = timeout_ns / 16u + 65536u;
@@ -183,11 +183,25 @@ __device__ __forceinline__ bool bounded_spin(Pred pred, uint64_t timeout_ns,
         if (sleep_ns < 512) sleep_ns <<= 1;
         if (pred()) return true;
         if ((it & 7u) == 0u) {
-            if (tag && ld_volatile_u32(status + kAbortWord) == tag) return false;
+            if (giveup && tag && ld_volatile_u32(giveup) == tag) return false;
             if (globaltimer_ns() - t0 > timeout_ns) return false;
         }
     }
     return false;
+}
+
+// Epochs of flag-synchronised launches live on the device: a one-thread
+// kernel bumps the window's epoch word in stream order before each such
+// launch (never to 0, the value of fresh flags), and the launch reads it at
+// start.  A launch recorded in a CUDA graph therefore gets a new epoch on
+// every replay.
+sym_status_t bump_epoch(uint32_t* epoch, cudaStream_t st);   // enqueues the bump
+
+__device__ __forceinline__ uint32_t read_epoch(const uint32_t* epoch) {
+    __shared__ uint32_t s_epoch;
+    if (threadIdx.x == 0) s_epoch = ld_volatile_u32(epoch);
+    __syncthreads();
+    return s_epoch;
 }
 
 // ----------------------------------------------------------------- bulk async copies (TMA engine)

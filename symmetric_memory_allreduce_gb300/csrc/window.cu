@@ -86,6 +86,11 @@ uint32_t pull_lag_waves() {
     return v;
 }
 
+bool test_drop_last_signal() {
+    static const bool v = env_u64("SYM_TEST_DROP_LAST_SIGNAL", 0) != 0;
+    return v;
+}
+
 bool twoshot_use_bulk() {
     static const bool v = [] {
         const char* s = getenv("SYM_TWOSHOT_KERNEL");
@@ -146,6 +151,18 @@ DevCtx* dev_ctx(int device) {
     return c;
 }
 
+__global__ void k_bump_epoch(uint32_t* epoch) {
+    uint32_t e = *epoch + 1u;
+    *epoch = e ? e : 1u;
+}
+
+sym_status_t bump_epoch(uint32_t* epoch, cudaStream_t st) {
+    k_bump_epoch<<<1, 1, 0, st>>>(epoch);
+    count_launch();
+    SYM_CUDA(cudaGetLastError());
+    return SYM_OK;
+}
+
 }  // namespace symar
 
 using namespace symar;
@@ -159,7 +176,7 @@ static sym_status_t alloc_aux(sym_window* w) {
     size_t cnt_b = sizeof(uint64_t) * (size_t)w->R * w->ncounters;
     size_t flg_b = sizeof(uint32_t) * (size_t)w->R * w->flag_tiles;
     size_t pair_b = sizeof(uint32_t) * (size_t)w->R * w->R;
-    size_t total = sig_b + cnt_b + 2 * flg_b + pair_b;
+    size_t total = sig_b + cnt_b + 2 * flg_b + pair_b + 2 * sizeof(uint32_t);
     char* p = nullptr;
     SYM_CUDA(cudaMalloc(&p, total));
     cudaError_t e = cudaMemset(p, 0, total);
@@ -173,7 +190,8 @@ static sym_status_t alloc_aux(sym_window* w) {
     w->flags = (uint32_t*)(p + sig_b + cnt_b);
     w->arrivals = (uint32_t*)(p + sig_b + cnt_b + flg_b);
     w->pair_arrivals = (uint32_t*)(p + sig_b + cnt_b + 2 * flg_b);
-    w->epoch = 0;
+    w->epoch = (uint32_t*)(p + sig_b + cnt_b + 2 * flg_b + pair_b);
+    w->giveup = w->epoch + 1;
     return SYM_OK;
 }
 
