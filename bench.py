@@ -488,13 +488,31 @@ def run_sweep(args) -> int:
             ts = [s.elapsed_time(e) for s, e in ev]
             med = statistics.median(ts)
             comp = algo_bytes(algo, R, nbytes)["compulsory"]
-            print(json.dumps({"bytes_per_rank": nbytes, "algo": algo, "iters": iters,
-                              "us_median": med * 1e3, "us_p10": percentile(ts, 0.1) * 1e3,
-                              "us_p90": percentile(ts, 0.9) * 1e3,
-                              "algbw_gbs": nbytes / (med * 1e-3) / 1e9,
-                              "hbm_gbs": comp / (med * 1e-3) / 1e9,
-                              "hbm_frac": comp / (med * 1e-3) / 1e9 / peak,
-                              "auto": sm.sym_allreduce_algo(send, n, "f32")}), flush=True)
+            row = {"bytes_per_rank": nbytes, "algo": algo, "iters": iters,
+                   "us_median": med * 1e3, "us_p10": percentile(ts, 0.1) * 1e3,
+                   "us_p90": percentile(ts, 0.9) * 1e3,
+                   "algbw_gbs": nbytes / (med * 1e-3) / 1e9,
+                   "hbm_gbs": comp / (med * 1e-3) / 1e9,
+                   "hbm_frac": comp / (med * 1e-3) / 1e9 / peak,
+                   "auto": sm.sym_allreduce_algo(send, n, "f32")}
+            if nbytes <= (1 << 20):
+                # device-side latency: 100 calls recorded in a CUDA graph, replayed
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for _ in range(100):
+                        sm.sym_allreduce(send, recv, n, "f32", "sum", algo)
+                g.replay()
+                torch.cuda.synchronize()
+                g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                g0.record(stream)
+                for _ in range(10):
+                    g.replay()
+                g1.record(stream)
+                torch.cuda.synchronize()
+                assert sm.sym_stream_status() == sm.SYM_OK
+                row["us_per_call_graph"] = g0.elapsed_time(g1) * 1e3 / 1000
+                del g
+            print(json.dumps(row), flush=True)
         send.free()
         recv.free()
     return 0
