@@ -219,10 +219,39 @@ def cpu_oracle_rate(x_sample, budget_s: float) -> dict:
         if el >= budget_s:
             break
     S = n * x_sample.itemsize
+    # the same rank-order sum on one thread, over a quarter of the budget
+    p1 = 0
+    t1 = time.perf_counter()
+    while True:
+        oracle.allreduce_sum_mt(x_sample, 1)
+        p1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= budget_s / 4:
+            break
     return {"value": S * passes / el / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
             "sample": f"R={R} x {n} fp32 elements per rank (first {S >> 20} MiB of each rank's "
                       f"256 MiB input), {passes} passes in {el:.1f} s, {used} threads",
-            "seconds_per_pass": el / passes}
+            "seconds_per_pass": el / passes, "single_thread_value": S * p1 / el1 / 1e9,
+            "cpu_model": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's name from /proc/cpuinfo (x86 'model name'; Arm implementer/part)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return f"Arm implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return "unknown"
 
 
 def run_reference(args) -> int:
@@ -256,7 +285,8 @@ def run_reference(args) -> int:
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded U(-1,1) fp32, PCG64)",
             "config": _config(R, N_DEFAULT, "oracle (CPU, rank order)"),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": used, "kind": "oracle",
-                             "sample": f"R={R} x {n_sample} fp32 elements per rank per step"},
+                             "sample": f"R={R} x {n_sample} fp32 elements per rank per step",
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -465,6 +495,7 @@ def run_sweep(args) -> int:
     peak, _ = measured_peak()
     sizes = [s for s in wl.SWEEP_BYTES if s <= args.sweep_max]
     algos = ["oneshot", "twoshot", "twoshot_pull", "twoshot_split"]
+    flush = _l2_flush_buffer()
     for nbytes in sizes:
         n = nbytes // 4
         x = wl.normal_f32(4, R, n)
@@ -495,6 +526,11 @@ def run_sweep(args) -> int:
                    "hbm_gbs": comp / (med * 1e-3) / 1e9,
                    "hbm_frac": comp / (med * 1e-3) / 1e9 / peak,
                    "auto": sm.sym_allreduce_algo(send, n, "f32")}
+            if 2 * R * nbytes <= L2_FLUSH_BYTES // 2:
+                # inputs + outputs fit in L2: also time with L2 flushed before each launch
+                cold = _time_launches(lambda: sm.sym_allreduce(send, recv, n, "f32", "sum", algo),
+                                      min(iters, 50), stream, flush)
+                row["us_median_cold"] = statistics.median(cold) * 1e3
             if nbytes <= (1 << 20):
                 # device-side latency: 100 calls recorded in a CUDA graph, replayed
                 g = torch.cuda.CUDAGraph()
@@ -518,8 +554,11 @@ def run_sweep(args) -> int:
     return 0
 
 
-def _time_launches(fn, iters: int, stream) -> list[float]:
-    """Per-launch CUDA-event times (ms) of fn() on `stream`, after 5 warm-ups."""
+def _time_launches(fn, iters: int, stream, flush=None) -> list[float]:
+    """Per-launch CUDA-event times (ms) of fn() on `stream`, after 5 warm-ups.
+
+    flush: a device buffer larger than L2, overwritten before every timed
+    launch (outside its events) so that the launch starts with a cold L2."""
     import torch
 
     for _ in range(5):
@@ -528,6 +567,8 @@ def _time_launches(fn, iters: int, stream) -> list[float]:
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(iters)]
     for s, e in ev:
+        if flush is not None:
+            flush.zero_()
         s.record(stream)
         fn()
         e.record(stream)
@@ -535,9 +576,20 @@ def _time_launches(fn, iters: int, stream) -> list[float]:
     return [s.elapsed_time(e) for s, e in ev]
 
 
+L2_FLUSH_BYTES = 256 << 20       # about twice the 126 MiB L2
+
+
+def _l2_flush_buffer():
+    import torch
+
+    return torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+
 def run_suite(args) -> int:
-    """Every hot-path row on its workload: one JSON object per (row, variant)."""
-    import numpy as np
+    """Every hot-path row on its workload: one JSON object per (row, variant).
+
+    --rows picks row groups, --scale divides every per-rank size (small cases
+    for profiler runs), --suite-iters fixes the timed launches per row."""
     import torch
 
     import symmetric_memory_allreduce_gb300 as sm
@@ -547,6 +599,7 @@ def run_suite(args) -> int:
     sm.load()
     stream = torch.cuda.current_stream()
     peak, peak_kind = measured_peak()
+    flush = _l2_flush_buffer()
 
     def report(row, variant, ts, per_rank, hbm_bytes, logical_bytes=None, extra=None):
         med = statistics.median(ts)
@@ -564,15 +617,26 @@ def run_suite(args) -> int:
         assert sm.sym_stream_status() == sm.SYM_OK, sm.sym_last_error()
 
     def iters_for(nbytes):
+        if args.suite_iters:
+            return args.suite_iters
         return max(20, min(1000, int(4e9 / max(nbytes, 1))))
+
+    def its(n):
+        return args.suite_iters or n
+
+    scale = max(1, args.scale)
+    wanted = [w.strip() for w in args.rows.split(",") if w.strip()]
+
+    def want(group):
+        return not wanted or group in wanted
 
     # AllReduce rows: configs 1-3 (fp32, bf16 where stated), every algorithm
     cases = [(1, "f32", ["oneshot", "twoshot", "twoshot_pull", "twoshot_split"]),
              (2, "f32", ["oneshot", "twoshot", "twoshot_pull", "twoshot_split"]),
              (3, "f32", ["twoshot", "twoshot_pull", "twoshot_split"]),
              (3, "bf16", ["twoshot", "twoshot_pull"])]
-    for cfg, dt, algos in cases:
-        x = wl.config_inputs(cfg)
+    for cfg, dt, algos in cases if want("allreduce") else []:
+        x = wl.config_inputs(cfg, n=wl.CONFIGS[cfg].count // scale)
         if dt == "bf16":
             x = wl.to_bf16_bits(x)
         R, n = x.shape
@@ -585,60 +649,91 @@ def run_suite(args) -> int:
             ts = _time_launches(lambda: sm.sym_allreduce(send, recv, n, dt, "sum", algo),
                                 iters_for(2 * R * S), stream)
             m = algo_bytes(algo, R, S)
+            resident = 2 * R * S < (126 << 20)
             report(f"allreduce config{cfg}", f"{algo} {dt}", ts, S, m["compulsory"], m["logical"],
-                   {"R": R, "bytes_per_rank": S, "l2_resident": 2 * R * S < (126 << 20)})
+                   {"R": R, "bytes_per_rank": S, "l2_resident": resident})
+            if resident:
+                # the same launches with L2 flushed before each one (cold column)
+                ts = _time_launches(lambda: sm.sym_allreduce(send, recv, n, dt, "sum", algo),
+                                    its(50), stream, flush)
+                report(f"allreduce config{cfg}", f"{algo} {dt} cold L2", ts, S, m["compulsory"],
+                       m["logical"], {"R": R, "bytes_per_rank": S, "l2_resident": False})
         send.free()
         recv.free()
         del x
 
     # AllGather (copy, CE) and put+signal AllGather: config 5
-    cfg5 = wl.PUT_SIGNAL
-    R, S = cfg5["R"], cfg5["nbytes"]
-    xb = wl.random_bytes(5, R, S)
-    send, recv = sm.Window(R, S, ncounters=1), sm.Window(R, R * S, nsignals=R)
-    for r in range(R):
-        send.write(r, xb[r])
-    stream.synchronize()
-    comp = R * S + R * R * S
-    for algo in ("copy", "ce"):
-        ts = _time_launches(lambda: sm.sym_allgather(send, recv, S // 4, "f32", algo), 50, stream)
-        report("allgather config5", algo, ts, S, comp, extra={"R": R, "bytes_per_rank": S})
-    for batch in (8, 1, 64):
-        ts = _time_launches(lambda: sm.sym_allgather(send, recv, S // 4, "f32", "put_signal",
-                                                     cfg5["chunk"], batch), 50, stream)
-        report("put_signal allgather config5", f"chunk 64KiB, {batch} chunks/signal", ts, S, comp,
-               extra={"R": R, "bytes_per_rank": S, "signals_per_pair": -(-512 // batch)})
-    send.free()
-    recv.free()
+    if want("allgather") or want("put_signal"):
+        cfg5 = wl.PUT_SIGNAL
+        R, S = cfg5["R"], cfg5["nbytes"] // scale
+        xb = wl.random_bytes(5, R, S)
+        send, recv = sm.Window(R, S, ncounters=1), sm.Window(R, R * S, nsignals=R)
+        for r in range(R):
+            send.write(r, xb[r])
+        stream.synchronize()
+        comp = R * S + R * R * S
+        for algo in ("copy", "ce") if want("allgather") else ():
+            ts = _time_launches(lambda: sm.sym_allgather(send, recv, S // 4, "f32", algo), its(50),
+                                stream)
+            kern = os.environ.get("SYM_ALLGATHER_KERNEL", "bulk") if algo == "copy" else "copy engines"
+            report("allgather config5", algo, ts, S, comp,
+                   extra={"R": R, "bytes_per_rank": S, "kernel": kern})
+        nchunks = -(-S // cfg5["chunk"])
+        for batch in (8, 1, 64) if want("put_signal") else ():
+            ts = _time_launches(lambda: sm.sym_allgather(send, recv, S // 4, "f32", "put_signal",
+                                                         cfg5["chunk"], batch), its(50), stream)
+            report("put_signal allgather config5", f"chunk 64KiB, {batch} chunks/signal", ts, S, comp,
+                   extra={"R": R, "bytes_per_rank": S, "signals_per_pair": -(-nchunks // batch)})
+        send.free()
+        recv.free()
 
     # AlltoAll: R=8, 32 MiB per rank (R segments of 4 MiB)
-    R, B = 8, 4 << 20
-    xa = wl.random_bytes(6, R, R * B)
-    send, recv = sm.Window(R, R * B), sm.Window(R, R * B, nsignals=1)
-    for r in range(R):
-        send.write(r, xa[r])
-    stream.synchronize()
-    for algo in ("copy", "put_signal"):
-        ts = _time_launches(lambda: sm.sym_alltoall(send, recv, B // 4, "f32", algo), 100, stream)
-        report("alltoall", algo, ts, R * B, 2 * R * R * B, extra={"R": R, "bytes_per_segment": B})
-    send.free()
-    recv.free()
+    if want("alltoall"):
+        R, B = 8, (4 << 20) // scale
+        xa = wl.random_bytes(6, R, R * B)
+        send, recv = sm.Window(R, R * B), sm.Window(R, R * B, nsignals=1)
+        for r in range(R):
+            send.write(r, xa[r])
+        stream.synchronize()
+        for algo in ("copy", "put_signal"):
+            ts = _time_launches(lambda: sm.sym_alltoall(send, recv, B // 4, "f32", algo), its(100),
+                                stream)
+            report("alltoall", algo, ts, R * B, 2 * R * R * B, extra={"R": R, "bytes_per_segment": B})
+        send.free()
+        recv.free()
 
     # fused producer + AllReduce: config-3 size
-    x = wl.config_inputs(3)
-    R, n = x.shape
-    S = n * 4
-    win_in, send, recv = sm.Window(R, S), sm.Window(R, S), sm.Window(R, S)
-    for r in range(R):
-        win_in.write(r, x[r])
-    stream.synchronize()
-    alpha = [1.0 + 0.25 * r for r in range(R)]
-    ts = _time_launches(lambda: sm.sym_scale_allreduce(win_in, send, recv, alpha, n), 100, stream)
-    report("fused producer + allreduce", "scale then two-shot, counter relay", ts, S, 3 * R * S,
-           extra={"R": R, "bytes_per_rank": S, "bytes_model": "read in RS + write contributions RS "
-                                                             "+ write results RS"})
-    for w in (win_in, send, recv):
-        w.free()
+    if want("fused"):
+        x = wl.config_inputs(3, n=wl.CONFIGS[3].count // scale)
+        R, n = x.shape
+        S = n * 4
+        win_in, send, recv = sm.Window(R, S), sm.Window(R, S), sm.Window(R, S)
+        for r in range(R):
+            win_in.write(r, x[r])
+        stream.synchronize()
+        alpha = [1.0 + 0.25 * r for r in range(R)]
+        ts = _time_launches(lambda: sm.sym_scale_allreduce(win_in, send, recv, alpha, n), its(100),
+                            stream)
+        report("fused producer + allreduce", "scale then two-shot, counter relay", ts, S,
+               3 * R * S, extra={"R": R, "bytes_per_rank": S,
+                                 "bytes_model": "read in RS + write contributions RS + write "
+                                                "results RS"})
+        for w in (win_in, send, recv):
+            w.free()
+
+    # practical ceilings on this GPU (library kernels, calibration only): an SM
+    # copy (reads = writes), a copy-engine copy, and a write-only fill, 2 GiB each
+    if want("ceiling"):
+        nb = (2 << 30) // scale
+        src = torch.empty(nb // 4, dtype=torch.float32, device="cuda").normal_()
+        dst = torch.empty_like(src)
+        ts = _time_launches(lambda: torch.mul(src, 1.0, out=dst), its(50), stream)
+        report("ceiling", "SM copy (torch elementwise)", ts, nb, 2 * nb, extra={"bytes": nb})
+        ts = _time_launches(lambda: dst.copy_(src), its(50), stream)
+        report("ceiling", "device copy (torch copy_)", ts, nb, 2 * nb, extra={"bytes": nb})
+        ts = _time_launches(lambda: dst.fill_(1.0), its(50), stream)
+        report("ceiling", "write only (torch fill_)", ts, nb, nb, extra={"bytes": nb})
+        del src, dst
     return 0
 
 
@@ -661,6 +756,13 @@ def parse(argv=None):
     ap.add_argument("--sweep-max", type=int, default=1 << 30)
     ap.add_argument("--suite", action="store_true",
                     help="time every hot-path row on its workload instead of the contract line")
+    ap.add_argument("--rows", default="",
+                    help="--suite: comma-separated row groups (allreduce, allgather, put_signal, "
+                         "alltoall, fused, ceiling); default all")
+    ap.add_argument("--scale", type=int, default=1,
+                    help="--suite: divide every per-rank size by this (small profiling cases)")
+    ap.add_argument("--suite-iters", type=int, default=0,
+                    help="--suite: timed launches per row (0: by size); small for profiler runs")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)          # at least three untimed warm-up steps
     return a

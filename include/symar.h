@@ -183,8 +183,10 @@ sym_status_t sym_allreduce_algo(sym_win_t send, size_t count, sym_dtype_t dtype,
  * i < S = sendcount*sizeof(dtype).  [SYMEX] Example 2: the receive buffer
  * holds sendcount*nranks elements and segment q holds rank q's data.
  * recv bytes_per_rank >= R*S.  send and recv must be different windows.
- * algo: AUTO or COPY (SM kernel: each segment tile read once, stored R
- * times), CE ([SYMEX] Example 2's copy-engine policy, CTAPolicy ZERO: no SM
+ * algo: AUTO or COPY (SM kernel: each 16 KiB segment tile is loaded once
+ * into shared memory by a bulk copy and stored to the R ranks by R bulk
+ * copies; env SYM_ALLGATHER_KERNEL=ldst selects a register load/store kernel
+ * instead), CE ([SYMEX] Example 2's copy-engine policy, CTAPolicy ZERO: no SM
  * is used; one cudaMemcpy2DAsync per destination rank gathers the R
  * segments), or PUT_SIGNAL (see sym_allgather_put_signal, with chunk_bytes
  * and chunks_per_signal; 0 selects 64 KiB and 8).  For COPY and CE the two

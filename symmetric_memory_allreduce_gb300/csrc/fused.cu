@@ -112,7 +112,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_scale_allreduce(FusedArgs a) {
                                         base + (size_t)(2 * h + 1) * kThreads};
                 const bool hok[2] = {hidx[0] < c1, hidx[1] < c1};
                 float acc[2][4];
-                reduce_vectors<F32T, OpSum, 4, 2, kLoadKeep>(a.send, a.sstride, a.R, hidx, hok, acc);
+                // last use of the contributions: streaming loads let their
+                // lines go first, ahead of contributions still to be reduced
+                reduce_vectors<F32T, OpSum, 4, 2, kLoadStream>(a.send, a.sstride, a.R, hidx, hok, acc);
                 const uint4 o0 = F32T::narrow(acc[0]), o1 = F32T::narrow(acc[1]);
                 for (int r = 0; r < a.R; ++r) {
                     char* dst = a.recv + (size_t)r * a.rstride;
@@ -185,7 +187,12 @@ extern "C" sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_wi
     const size_t per_block = (size_t)a.R * a.R + a.R;
     const size_t slots = per_block * a.tiles_per_chunk;
     const size_t grid = std::min(std::max(slots, (size_t)1), cap);
-    a.lag = (uint32_t)(pull_lag_waves() * ceil_div(grid, per_block)) + 1;
+    // consumers trail producers by a few grid waves: 64 KiB relay tiles make
+    // one tile block R*R*64 KiB of contributions, which should still be in L2
+    // when the consumer reads them back (at 8 waves an ncu capture showed them
+    // re-read from DRAM; 3 waves timed fastest, 1 too few to hide the
+    // producers' latency)
+    a.lag = (uint32_t)(fused_lag_waves() * ceil_div(grid, per_block)) + 1;
     void* args[] = {&a};
     // consumers wait on producers of the same launch -> co-residency required
     SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_scale_allreduce, dim3((unsigned)grid),

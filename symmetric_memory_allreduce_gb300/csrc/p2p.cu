@@ -61,6 +61,72 @@ __global__ void __launch_bounds__(kCopyThreads) k_allgather_copy(AgArgs a) {
     }
 }
 
+// AllGather staged through shared memory by the TMA engine.  Each tile of
+// segment q is read once by a bulk load (mbarrier completion) and written to
+// all R ranks by R bulk stores from shared memory, so the SM's load/store
+// queues carry none of the R-fold stores (the register version stalls on
+// them).  One thread drives a ring of kAgStages tiles, loads running
+// kAgStages - 1 tiles ahead of the stores.  Needs S % 16 == 0.
+constexpr int kAgStages = 4;
+constexpr uint32_t kAgTile = 16384;
+constexpr int kAgThreads = 32;
+constexpr size_t kAgSmem = (size_t)kAgStages * kAgTile + 64;
+
+__global__ void __launch_bounds__(kAgThreads) k_allgather_bulk(AgArgs a, uint32_t* status) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kAgStages * kAgTile);
+    if (threadIdx.x != 0) return;
+    const uint32_t R = (uint32_t)a.R, items = R * a.tiles;
+    const uint32_t nmine = blockIdx.x < items ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    auto item = [&](uint32_t i, uint32_t& q, size_t& off, uint32_t& bytes) {
+        const uint32_t w = blockIdx.x + i * gridDim.x;
+        const uint32_t t = w / R;
+        q = w - t * R;
+        off = (size_t)t * kAgTile;
+        bytes = (uint32_t)min((size_t)kAgTile, a.S - off);
+    };
+    auto load = [&](uint32_t i) {
+        uint32_t q, bytes;
+        size_t off;
+        item(i, q, off, bytes);
+        const int s = (int)(i % kAgStages);
+        mbar_expect_tx(&full[s], bytes);
+        bulk_load(smem + (size_t)s * kAgTile, a.send + (size_t)q * a.sstride + off, bytes, &full[s]);
+    };
+    for (int s = 0; s < kAgStages; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+    for (uint32_t i = 0; i + 1 < (uint32_t)kAgStages && i < nmine; ++i) load(i);
+    for (uint32_t i = 0; i < nmine; ++i) {
+        const int s = (int)(i % kAgStages);
+        uint32_t spins = 0;
+        bool ok = true;
+        while (!mbar_try_wait(&full[s], (i / kAgStages) & 1u)) {
+            if (++spins > (1u << 26)) {          // bounded: a load cannot stall on valid ranges
+                ok = false;
+                break;
+            }
+        }
+        if (!ok) {
+            report_timeout(status, nullptr, 0u, kSiteBulkStage, blockIdx.x, i);
+            break;
+        }
+        uint32_t q, bytes;
+        size_t off;
+        item(i, q, off, bytes);
+        for (uint32_t r = 0; r < R; ++r)
+            bulk_store(a.recv + (size_t)r * a.rstride + (size_t)q * a.S + off,
+                       smem + (size_t)s * kAgTile, bytes);
+        bulk_commit();
+        // refill the stage of item i-1 (its stores are the older groups)
+        const uint32_t nxt = i + kAgStages - 1;
+        if (nxt < nmine) {
+            bulk_wait_read<1>();
+            load(nxt);
+        }
+    }
+    bulk_wait_all<0>();
+}
+
 // Byte-granular fallback when S is not a multiple of 16.
 __global__ void k_allgather_bytes(AgArgs a) {
     const size_t total = (size_t)a.R * a.S;
@@ -448,7 +514,16 @@ sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym
     a.R = R;
     a.S = S;
     const int sms = recv->ctx->num_sms;
-    if (S % 16 == 0) {
+    if (S % 16 == 0 && allgather_use_bulk()) {
+        a.nvec = S / 16;
+        a.tiles = (uint32_t)ceil_div(S, (size_t)kAgTile);
+        SYM_CUDA(cudaFuncSetAttribute((const void*)k_allgather_bulk,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAgSmem));
+        const size_t items = (size_t)R * a.tiles;
+        const int occ = occupancy((const void*)k_allgather_bulk, kAgThreads, kAgSmem);
+        const size_t grid = std::min(items, (size_t)std::max(occ, 1) * sms);
+        k_allgather_bulk<<<(unsigned)grid, kAgThreads, kAgSmem, st>>>(a, recv->ctx->status);
+    } else if (S % 16 == 0) {
         a.nvec = S / 16;
         a.tiles = (uint32_t)ceil_div(a.nvec, (size_t)kCopyThreads * kCopyU);
         const size_t items = (size_t)R * a.tiles;

@@ -99,9 +99,11 @@ bool trace_on();
 uint64_t default_timeout_ns();
 size_t oneshot_max_bytes();
 bool twoshot_use_bulk();          // env SYM_TWOSHOT_KERNEL=bulk|ldst
+bool allgather_use_bulk();        // env SYM_ALLGATHER_KERNEL=bulk (default)|ldst
 // Grid waves between a tile's producing item and the items that wait for it
 // (flag-synchronised kernels); env SYM_PULL_LAG_WAVES, default 4, 1..64.
 uint32_t pull_lag_waves();
+uint32_t fused_lag_waves();       // the same for the fused producer; env SYM_FUSED_LAG_WAVES, default 3
 // Fault injection for failure-detection tests (env SYM_TEST_DROP_LAST_SIGNAL=1):
 // the put + signal AllGather's (0 -> 0) stream omits its last signal, so its
 // receiver's bounded wait runs out.  Off by default; never needs a GPU fault.

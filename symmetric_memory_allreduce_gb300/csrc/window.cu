@@ -100,6 +100,22 @@ bool twoshot_use_bulk() {
     return v;
 }
 
+uint32_t fused_lag_waves() {
+    static const uint32_t v = [] {
+        uint64_t w = env_u64("SYM_FUSED_LAG_WAVES", 3);
+        return (uint32_t)(w < 1 ? 1 : (w > 64 ? 64 : w));
+    }();
+    return v;
+}
+
+bool allgather_use_bulk() {
+    static const bool v = [] {
+        const char* s = getenv("SYM_ALLGATHER_KERNEL");
+        return !(s && strcmp(s, "ldst") == 0);
+    }();
+    return v;
+}
+
 size_t dtype_size(sym_dtype_t t) {
     switch (t) {
         case SYM_F32: return 4;
