@@ -34,7 +34,10 @@
  *    puts need not be multiples of 16; 16-byte multiples take the vector path.
  *  - Device-side waits are bounded (default 2 s, env SYM_TIMEOUT_NS).  A wait
  *    that runs out sets the device's status word and returns; the host sees it
- *    as SYM_ERR_TIMEOUT from sym_stream_status().  No call traps the GPU.
+ *    as SYM_ERR_TIMEOUT from sym_stream_status(); sym_last_error() then names
+ *    the wait site: 1 signal wait, 2 counter wait, 3 pull-tile flag, 4 put +
+ *    signal / AlltoAll receiver, 5 bulk-copy stage, 6 put + signal batch
+ *    order.  No call traps the GPU.
  *  - Windows are owned by the library (sym_window_alloc) or by the caller
  *    (sym_window_register).  Free a window only after every stream that used
  *    it has finished with it; windows must be freed before unloading.
@@ -187,8 +190,8 @@ sym_status_t sym_allreduce_algo(sym_win_t send, size_t count, sym_dtype_t dtype,
  * into shared memory by a bulk copy and stored to the R ranks by R bulk
  * copies; env SYM_ALLGATHER_KERNEL=ldst selects a register load/store kernel
  * instead), CE ([SYMEX] Example 2's copy-engine policy, CTAPolicy ZERO: no SM
- * is used; one cudaMemcpy2DAsync per destination rank gathers the R
- * segments), or PUT_SIGNAL (see sym_allgather_put_signal, with chunk_bytes
+ * is used; R*R cudaMemcpyAsync copies, one per (sender, destination)
+ * pair, sender-major), or PUT_SIGNAL (see sym_allgather_put_signal, with chunk_bytes
  * and chunks_per_signal; 0 selects 64 KiB and 8).  For COPY and CE the two
  * chunk arguments are ignored. */
 sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym_dtype_t dtype,
@@ -207,12 +210,15 @@ sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym
  * of every rank of `recv` and counter slot 0 of every rank of `send` are set
  * to 0 first (stream-ordered), so afterwards signal[p][q] ==
  * ceil(ceil(S/chunk)/batch) and counter[q] == R*ceil(S/chunk).
+ * Batches of different (q, p) streams run in parallel; the signals of one
+ * stream are added in batch order (the put of batch k waits, bounded, until
+ * the stream's signal reads k).
  * The same launch holds the receivers: each (p, q) waits (bounded by
  * timeout_ns, 0 = default) until its signal reaches that count.
  * If d_mismatch (device pointer to one uint64) is not NULL, receivers check
- * prefix visibility while they wait: each time a signal grows from a to b
- * they compare batches a..b-1 with the source and add differing bytes to
- * *d_mismatch (expected 0).  Requires recv nsignals >= R, send ncounters >= 1.
+ * prefix visibility while the senders run: once signal[p][q] reads k+1 they
+ * compare batch k with the source and add differing bytes to *d_mismatch
+ * (expected 0).  Requires recv nsignals >= R, send ncounters >= 1.
  * If one receiver's wait runs out, the launch's other waits stop early (each
  * launch is tagged with the recv window's device epoch).  For failure tests,
  * env SYM_TEST_DROP_LAST_SIGNAL=1 makes the (0 -> 0) stream omit its last

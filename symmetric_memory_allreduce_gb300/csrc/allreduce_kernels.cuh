@@ -537,6 +537,8 @@ __global__ void __launch_bounds__(kThreads, pull_blocks_per_sm<T, Op>()) k_twosh
     // tile b and the gather items of tile b - lag.
     const uint32_t ep = read_epoch(a.epoch_ptr);
     const uint64_t total = (uint64_t)(T_ + a.lag) * RR;
+    // static stride: an ordered ticket (as in the fused producer) measured
+    // 4 % slower here, the gathers waiting on reductions still in flight
     for (uint64_t w = blockIdx.x; w < total; w += gridDim.x) {
         const uint32_t b = (uint32_t)(w / RR), s = (uint32_t)(w - (uint64_t)b * RR);
         if (s < R) {

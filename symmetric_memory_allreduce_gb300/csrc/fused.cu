@@ -30,6 +30,7 @@ struct FusedArgs {
     uint32_t lag;
     uint32_t* status;
     uint32_t* giveup;        // the recv window's give-up word
+    unsigned long long* ticket;   // the recv window's item ticket, zeroed before the launch
     uint64_t timeout_ns;
     float alpha[kMaxRanks];
 };
@@ -50,7 +51,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_scale_allreduce(FusedArgs a) {
     const uint32_t per_block = R * R + R;
     uint32_t parity = 0;
     const uint64_t total = (uint64_t)(T_ + a.lag) * per_block;
-    for (uint64_t w = blockIdx.x; w < total; w += gridDim.x) {
+    __shared__ unsigned long long s_item[2];
+    int ipar = 0;
+    for (;;) {
+        const uint64_t w = fetch_item(a.ticket, s_item, ipar);
+        if (w >= total) break;
         const uint32_t b = (uint32_t)(w / per_block), s = (uint32_t)(w - (uint64_t)b * per_block);
         const bool producer = s < R * R;
         const uint32_t t = producer ? b : b - a.lag;
@@ -172,10 +177,11 @@ extern "C" sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_wi
     if (!g.ok) return SYM_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
     {
-        sym_status_t s = bump_epoch(recv->epoch, st);
+        sym_status_t s = bump_epoch(recv->epoch, st, recv->ticket);
         if (s != SYM_OK) return s;
     }
     a.epoch = recv->epoch;
+    a.ticket = recv->ticket;
     a.flags = recv->flags;
     a.arrivals = recv->arrivals;
     a.flag_stride = recv->flag_tiles;
@@ -187,12 +193,15 @@ extern "C" sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_wi
     const size_t per_block = (size_t)a.R * a.R + a.R;
     const size_t slots = per_block * a.tiles_per_chunk;
     const size_t grid = std::min(std::max(slots, (size_t)1), cap);
-    // consumers trail producers by a few grid waves: 64 KiB relay tiles make
-    // one tile block R*R*64 KiB of contributions, which should still be in L2
-    // when the consumer reads them back (at 8 waves an ncu capture showed them
-    // re-read from DRAM; 3 waves timed fastest, 1 too few to hide the
-    // producers' latency)
-    a.lag = (uint32_t)(fused_lag_waves() * ceil_div(grid, per_block)) + 1;
+    // consumers trail producers by about one grid wave of items (the whole
+    // tile blocks that fit in it): long enough that a consumer seldom waits
+    // for producers still in flight, short enough that the contributions it
+    // reads back are still in L2.  Items are handed out in index order by
+    // the window's ticket, so a consumer only waits for producer items that
+    // running blocks already hold.  On GB300 (R = 8: 304 blocks, 72 items a
+    // tile block) 3-4 blocks measured fastest; 8 was 5 % slower.
+    const int64_t lb = fused_lag_blocks();
+    a.lag = lb >= 0 ? (uint32_t)lb : (uint32_t)std::max<size_t>(1, grid / per_block);
     void* args[] = {&a};
     // consumers wait on producers of the same launch -> co-residency required
     SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_scale_allreduce, dim3((unsigned)grid),

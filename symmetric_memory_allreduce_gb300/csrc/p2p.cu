@@ -151,7 +151,13 @@ struct PsArgs {
     uint64_t* cnt;            // send window counters [R][ncnt]
     uint32_t ncnt;
     uint64_t* mismatch;       // optional prefix-visibility check
-    uint32_t nproducers;      // CTAs [0, nproducers) put; the rest only receive
+    unsigned long long* ticket;   // recv window item ticket, zeroed by the reset kernel
+    uint32_t* ring;           // recv window [R][R][2] piece counters by batch parity
+    // item geometry (see k_put_signal_allgather)
+    uint32_t nrows;           // rows of items
+    uint32_t bpr;             // batches per row (ppi == 1), else 1
+    uint32_t ppi;             // items per stream in a row (pieces of one batch), 1 = whole batches
+    uint32_t gchunks;         // chunks per piece when ppi > 1
     uint32_t* status;
     const uint32_t* epoch;    // recv window epoch (this launch's give-up tag)
     uint32_t* giveup;         // recv window give-up word
@@ -173,78 +179,130 @@ __device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* s_red) {
     return t;
 }
 
+// Work items are handed out in index order by the window's ticket
+// (fetch_item) and move about 512 KiB each, whatever the batch size: in a row
+// of items, every (q -> p) stream has either one item that puts `bpr` whole
+// batches (small batches), or `ppi` items that each put a piece of one batch
+// (large batches).  With the prefix check on, each row ends with one check
+// item per stream; with it off, one receiver item per stream follows the last
+// row and waits for the final count.
+//
+// A batch's signal must follow the previous batch's signal of the same
+// stream: the item that completes batch b first waits (acquire) until the
+// stream's signal reads b, then adds 1 with a release, so a receiver that
+// reads k sees batches 0..k-1 (each release carries the earlier ones by
+// causality).  Pieces of a batch count their arrivals in a two-entry ring per
+// stream (by batch parity); a piece of batch b first waits until batch b-2 is
+// signalled, which frees its ring entry.  Every wait is for items handed out
+// earlier, which running blocks hold, so no wait depends on a block that has
+// not started.
 __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) {
-    __shared__ uint64_t s_v[2];
+    __shared__ unsigned long long s_item[2];
+    __shared__ int s_ok[2];
     __shared__ uint64_t s_red[kPutThreads / 32];
     const uint32_t tag = read_epoch(a.epoch);      // bumped by the reset kernel before
     const uint32_t R = (uint32_t)a.R, pairs = R * R;
-    // ---- senders: one CTA streams all batches of a (q -> p) pair in order
-    if (blockIdx.x < a.nproducers) {
-        for (uint32_t pr = blockIdx.x; pr < pairs; pr += a.nproducers) {
+    const uint64_t puts = (uint64_t)pairs * a.ppi;
+    const uint64_t row = puts + (a.mismatch ? pairs : 0u);
+    const uint64_t total = row * a.nrows + (a.mismatch ? 0ull : (uint64_t)pairs);
+    int ipar = 0, opar = 0;
+    auto sig_at = [&](uint32_t p, uint32_t q) { return a.sig + (size_t)p * a.nsig + q; };
+    for (;;) {
+        const uint64_t w = fetch_item(a.ticket, s_item, ipar);
+        if (w >= total) break;
+        const uint32_t r = (uint32_t)(w / row);
+        const uint64_t slot = w - (uint64_t)r * row;
+        // batches [b0, b1) of this row
+        const uint32_t b0 = r * a.bpr, b1 = min(b0 + a.bpr, a.nbatches);
+        if (r < a.nrows && slot < puts) {
+            // ---- a put item: stream (q -> p), piece j
+            // streams vary fastest: the items in flight cover one piece of many streams
+            const uint32_t j = (uint32_t)(slot / pairs), pr = (uint32_t)(slot - (uint64_t)j * pairs);
             const uint32_t p = pr / R, q = pr - p * R;
+            uint32_t k0, k1;                      // chunks
+            if (a.ppi == 1) {
+                k0 = b0 * a.B;
+                k1 = min(b1 * a.B, a.nchunks);
+            } else {
+                k0 = min(b0 * a.B + j * a.gchunks, a.nchunks);
+                k1 = min(min(k0 + a.gchunks, (b0 + 1) * a.B), a.nchunks);
+            }
             const char* src = a.send + (size_t)q * a.sstride;
             char* dst = a.recv + (size_t)p * a.rstride + (size_t)q * a.S;
-            for (uint32_t b = 0; b < a.nbatches; ++b) {
-                const uint32_t k0 = b * a.B, k1 = min(k0 + a.B, a.nchunks);
-                const size_t lo = (size_t)k0 * a.chunk, hi = min((size_t)k1 * a.chunk, a.S);
-                block_copy<kPutThreads, kPutU>(src, dst, lo, hi, a.vec != 0);
-                __syncthreads();
-                if (threadIdx.x == 0) {
-                    __threadfence();
+            const size_t lo = min((size_t)k0 * a.chunk, a.S), hi = min((size_t)k1 * a.chunk, a.S);
+            block_copy<kPutThreads, kPutU>(src, dst, lo, hi, a.vec != 0);
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                if (k1 > k0)
                     atomicAdd(reinterpret_cast<unsigned long long*>(a.cnt + (size_t)q * a.ncnt),
                               (unsigned long long)(k1 - k0));          // local completion
-                    const bool dropped = a.drop_last_signal && pr == 0 && b + 1 == a.nbatches;
-                    if (!dropped) red_release_add_u64(a.sig + (size_t)p * a.nsig + q, 1ull);
+                uint64_t* sp = sig_at(p, q);
+                bool last = true, ok = true;
+                if (a.ppi > 1) {
+                    // free ring entry: batch b0-2 signalled
+                    const uint64_t need = b0 >= 2 ? b0 - 1 : 0;
+                    ok = need == 0 || bounded_spin([&] { return ld_acquire_u64(sp) >= need; },
+                                                   a.timeout_ns, a.giveup, tag);
+                    if (ok) {
+                        uint32_t* cnt = a.ring + ((size_t)pr << 1) + (b0 & 1u);
+                        last = atomicAdd(cnt, 1u) == a.ppi - 1;
+                        if (last) {
+                            *cnt = 0;
+                            __threadfence();
+                        }
+                    }
                 }
+                if (ok && last) {
+                    const uint64_t before = b0;
+                    ok = b0 == 0 || bounded_spin([&] { return ld_acquire_u64(sp) >= before; },
+                                                 a.timeout_ns, a.giveup, tag);
+                    // one release pattern (fence, then strong adds) covers the
+                    // batches' bytes and the acquired predecessor; one add per batch
+                    if (ok) __threadfence();
+                    for (uint32_t b = b0; ok && b < b1; ++b) {
+                        const bool dropped = a.drop_last_signal && pr == 0 && b + 1 == a.nbatches;
+                        if (!dropped) red_relaxed_add_u64(sp, 1ull);
+                    }
+                }
+                if (!ok) report_timeout(a.status, a.giveup, tag, kSiteSignalChain, p, q);
             }
-        }
-    }
-    // ---- receivers: wait on every (p, q) signal; optionally check prefixes
-    const bool dedicated = a.nproducers < gridDim.x;
-    const uint32_t w0 = dedicated ? blockIdx.x - a.nproducers : blockIdx.x;
-    const uint32_t ws = dedicated ? gridDim.x - a.nproducers : gridDim.x;
-    if (dedicated && blockIdx.x < a.nproducers) return;
-    uint32_t parity = 0;
-    for (uint32_t pr = w0; pr < pairs; pr += ws) {
-        const uint32_t p = pr / R, q = pr - p * R;
-        const uint64_t* sp = a.sig + (size_t)p * a.nsig + q;
-        if (!a.mismatch) {
+        } else if (r < a.nrows) {
+            // ---- check: once the signal shows batch b1-1, batches [b0, b1) equal the source
+            const uint32_t pr = (uint32_t)(slot - puts), p = pr / R, q = pr - p * R;
             if (threadIdx.x == 0) {
-                const uint64_t want = a.nbatches;
-                if (!bounded_spin([&] { return ld_acquire_u64(sp) >= want; }, a.timeout_ns,
-                                  a.giveup, tag))
-                    report_timeout(a.status, a.giveup, tag, kSitePutSignalRecv, p, q);
-            }
-            continue;
-        }
-        const char* src = a.send + (size_t)q * a.sstride;
-        const char* seg = a.recv + (size_t)p * a.rstride + (size_t)q * a.S;
-        uint64_t seen = 0;
-        while (seen < a.nbatches) {
-            if (threadIdx.x == 0) {
-                uint64_t v = 0;
-                const uint64_t s0 = seen;
-                bool got = bounded_spin([&] { return (v = ld_acquire_u64(sp)) > s0; },
-                                        a.timeout_ns, a.giveup, tag);
+                const uint64_t* sp = sig_at(p, q);
+                const uint64_t want = b1;
+                const bool got = bounded_spin([&] { return ld_acquire_u64(sp) >= want; },
+                                              a.timeout_ns, a.giveup, tag);
                 if (!got) report_timeout(a.status, a.giveup, tag, kSitePutSignalRecv, p, q);
-                s_v[parity] = got ? min(v, (uint64_t)a.nbatches) : ~0ull;
+                s_ok[opar] = got ? 1 : 0;
             }
             __syncthreads();
-            const uint64_t v = s_v[parity];
-            parity ^= 1u;
-            if (v == ~0ull) break;
-            // batches [seen, v) must already equal the source
-            const size_t lo = (size_t)seen * a.B * a.chunk;
-            const size_t hi = min((size_t)v * a.B * a.chunk, a.S);
+            const bool go = s_ok[opar] != 0;
+            opar ^= 1;
+            if (!go) continue;
+            const char* src = a.send + (size_t)q * a.sstride;
+            const char* seg = a.recv + (size_t)p * a.rstride + (size_t)q * a.S;
+            const size_t lo = min((size_t)b0 * a.B * a.chunk, a.S);
+            const size_t hi = min((size_t)b1 * a.B * a.chunk, a.S);
             uint64_t bad = 0;
             for (size_t i = lo + threadIdx.x; i < hi; i += kPutThreads)
                 bad += (__ldcg(reinterpret_cast<const unsigned char*>(seg + i)) !=
                         __ldcg(reinterpret_cast<const unsigned char*>(src + i)));
             bad = block_sum_u64(bad, s_red);
             if (threadIdx.x == 0 && bad)
-                atomicAdd(reinterpret_cast<unsigned long long*>(a.mismatch),
-                          (unsigned long long)bad);
-            seen = v;
+                atomicAdd(reinterpret_cast<unsigned long long*>(a.mismatch), (unsigned long long)bad);
+        } else {
+            // ---- receiver (check off): wait for the stream's final count
+            const uint32_t pr = (uint32_t)slot, p = pr / R, q = pr - p * R;
+            if (threadIdx.x == 0) {
+                const uint64_t* sp = sig_at(p, q);
+                const uint64_t want = a.nbatches;
+                if (!bounded_spin([&] { return ld_acquire_u64(sp) >= want; }, a.timeout_ns,
+                                  a.giveup, tag))
+                    report_timeout(a.status, a.giveup, tag, kSitePutSignalRecv, p, q);
+            }
         }
     }
 }
@@ -269,7 +327,7 @@ struct A2aArgs {
     uint64_t* sig;            // recv window signals, slot 0 of each rank (put+signal form)
     uint32_t nsig;
     uint32_t* pair_done;      // [R][R] parts completed, zero when idle (put+signal form)
-    uint32_t nproducers;
+    unsigned long long* ticket;   // recv window item ticket (put+signal form)
     uint32_t* status;
     const uint32_t* epoch;    // recv window epoch (put+signal form: the give-up tag)
     uint32_t* giveup;         // recv window give-up word
@@ -277,34 +335,48 @@ struct A2aArgs {
 };
 
 __global__ void __launch_bounds__(kPutThreads) k_alltoall(A2aArgs a) {
-    const uint32_t tag = a.sig ? read_epoch(a.epoch) : 0u;   // uniform: a.sig is per launch
     const uint32_t R = (uint32_t)a.R, items = R * R * a.pieces;
-    if (blockIdx.x < a.nproducers) {
-        for (uint32_t it = blockIdx.x; it < items; it += a.nproducers) {
-            const uint32_t pr = it / a.pieces, part = it - pr * a.pieces;
-            const uint32_t q = pr / R, p = pr - q * R;
-            const char* src = a.send + (size_t)q * a.sstride + (size_t)p * a.B;
-            char* dst = a.recv + (size_t)p * a.rstride + (size_t)q * a.B;
-            const size_t lo = min((size_t)part * a.piece, a.B), hi = min(lo + a.piece, a.B);
-            block_copy<kPutThreads, kPutU>(src, dst, lo, hi, a.vec != 0);
-            if (a.sig) {
-                __syncthreads();
-                if (threadIdx.x == 0) {
+    auto put_part = [&](uint32_t it, uint32_t& q, uint32_t& p) {
+        const uint32_t pr = it / a.pieces, part = it - pr * a.pieces;
+        q = pr / R;
+        p = pr - q * R;
+        const char* src = a.send + (size_t)q * a.sstride + (size_t)p * a.B;
+        char* dst = a.recv + (size_t)p * a.rstride + (size_t)q * a.B;
+        const size_t lo = min((size_t)part * a.piece, a.B), hi = min(lo + a.piece, a.B);
+        block_copy<kPutThreads, kPutU>(src, dst, lo, hi, a.vec != 0);
+    };
+    if (!a.sig) {                                    // copy form: one part per block
+        for (uint32_t it = blockIdx.x; it < items; it += gridDim.x) {
+            uint32_t q, p;
+            put_part(it, q, p);
+        }
+        return;
+    }
+    // put + signal form: parts, then one receiver item per rank, handed out in
+    // index order by the window's ticket (receivers wait only on parts that
+    // running blocks already hold)
+    const uint32_t tag = read_epoch(a.epoch);
+    __shared__ unsigned long long s_item[2];
+    int ipar = 0;
+    for (;;) {
+        const uint64_t w = fetch_item(a.ticket, s_item, ipar);
+        if (w >= (uint64_t)items + R) break;
+        if (w < items) {
+            uint32_t q, p;
+            put_part((uint32_t)w, q, p);
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                uint32_t* done = a.pair_done + (size_t)q * R + p;
+                if (atomicAdd(done, 1u) == a.pieces - 1) {     // last part of the segment
+                    *done = 0;
                     __threadfence();
-                    uint32_t* done = a.pair_done + (size_t)q * R + p;
-                    if (atomicAdd(done, 1u) == a.pieces - 1) {     // last part of the segment
-                        *done = 0;
-                        __threadfence();
-                        red_release_add_u64(a.sig + (size_t)p * a.nsig, 1ull);
-                    }
+                    red_release_add_u64(a.sig + (size_t)p * a.nsig, 1ull);
                 }
             }
-        }
-    }
-    if (!a.sig) return;
-    // receivers: rank p waits until all R senders have signalled
-    for (uint32_t p = blockIdx.x; p < R; p += gridDim.x) {
-        if (threadIdx.x == 0) {
+        } else if (threadIdx.x == 0) {
+            // receiver: rank p waits until all R senders have signalled
+            const uint32_t p = (uint32_t)(w - items);
             const uint64_t* sp = a.sig + (size_t)p * a.nsig;
             if (!bounded_spin([&] { return ld_acquire_u64(sp) >= (uint64_t)R; }, a.timeout_ns,
                               a.giveup, tag))
@@ -322,18 +394,21 @@ __device__ __forceinline__ void bump_epoch_here(uint32_t* epoch) {
     }
 }
 
-__global__ void k_reset_slot0(uint64_t* sig, uint32_t nsig, int R, uint32_t* epoch) {
+__global__ void k_reset_slot0(uint64_t* sig, uint32_t nsig, int R, uint32_t* epoch,
+                              unsigned long long* ticket) {
     for (int p = threadIdx.x; p < R; p += blockDim.x) sig[(size_t)p * nsig] = 0;
+    if (threadIdx.x == 0) *ticket = 0ull;
     bump_epoch_here(epoch);
 }
 
 __global__ void k_reset_slots(uint64_t* sig, uint32_t nsig, uint64_t* cnt, uint32_t ncnt, int R,
-                              uint32_t* epoch) {
+                              uint32_t* epoch, unsigned long long* ticket) {
     for (int i = threadIdx.x; i < R * R; i += blockDim.x) {
         const int p = i / R, q = i - p * R;
         sig[(size_t)p * nsig + q] = 0;
     }
     for (int q = threadIdx.x; q < R; q += blockDim.x) cnt[(size_t)q * ncnt] = 0;
+    if (threadIdx.x == 0) *ticket = 0ull;
     bump_epoch_here(epoch);
 }
 
@@ -420,27 +495,37 @@ static sym_status_t launch_put_signal_allgather(sym_win_t send, sym_win_t recv, 
     if (a.timeout_ns > 60000000000ull) a.timeout_ns = 60000000000ull;
     a.vec = (S % 16 == 0 && chunk % 16 == 0) ? 1 : 0;
     a.drop_last_signal = test_drop_last_signal() ? 1 : 0;
-    k_reset_slots<<<1, 256, 0, st>>>(a.sig, a.nsig, a.cnt, a.ncnt, R, recv->epoch);
+    a.ticket = recv->ticket;
+    a.ring = recv->pair_ring;
+    // about 512 KiB per item: whole batches when a batch is at most that
+    const size_t gch = std::max<size_t>(1, (512 * 1024) / chunk);
+    if (B <= gch) {
+        a.bpr = (uint32_t)std::max<size_t>(1, gch / B);
+        a.ppi = 1;
+        a.gchunks = 0;
+        a.nrows = (uint32_t)ceil_div(a.nbatches, (size_t)a.bpr);
+    } else {
+        a.bpr = 1;
+        a.ppi = (uint32_t)ceil_div((size_t)B, gch);
+        a.gchunks = (uint32_t)gch;
+        a.nrows = a.nbatches;
+    }
+    k_reset_slots<<<1, 256, 0, st>>>(a.sig, a.nsig, a.cnt, a.ncnt, R, recv->epoch, recv->ticket);
     count_launch();
     const int occ = occupancy((const void*)k_put_signal_allgather, kPutThreads, 0);
     const size_t cap = (size_t)occ * recv->ctx->num_sms;
     const size_t pairs = (size_t)R * R;
-    size_t waiters = d_mismatch ? std::min(pairs, std::max(cap / 2, (size_t)1)) : 0;
-    size_t producers = std::min(pairs, cap - waiters);
-    if (producers == 0) {
-        producers = 1;
-        waiters = cap > 1 ? 1 : 0;
-    }
-    a.nproducers = (uint32_t)producers;
-    const size_t grid = producers + waiters;
+    const size_t items = (pairs * a.ppi + (d_mismatch ? pairs : 0)) * a.nrows + (d_mismatch ? 0 : pairs);
+    const size_t grid = std::max<size_t>(1, std::min(items, cap));
     void* args[] = {&a};
-    // receivers wait on senders in the same launch -> co-residency required
+    // all blocks resident (cooperative launch); the ticket order alone already
+    // keeps every wait on items that running blocks hold
     SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_put_signal_allgather, dim3((unsigned)grid),
                                          dim3(kPutThreads), args, 0, st));
     count_launch();
     if (trace_on())
-        fprintf(stderr, "[symar] put_signal_allgather R=%d S=%zu chunk=%zu B=%u grid=%zu+%zu\n", R,
-                S, chunk, B, producers, waiters);
+        fprintf(stderr, "[symar] put_signal_allgather R=%d S=%zu chunk=%zu B=%u grid=%zu items=%zu\n",
+                R, S, chunk, B, grid, items);
     return SYM_OK;
 }
 
@@ -465,11 +550,16 @@ sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym
     if (!g.ok) return SYM_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
     if (algo == SYM_ALGO_CE) {
-        // destination r receives the R segments back to back: a 2-D copy whose
-        // rows are the senders (source pitch = window stride, dest pitch = S)
-        for (int r = 0; r < R; ++r)
-            SYM_CUDA(cudaMemcpy2DAsync(recv->base + (size_t)r * recv->stride, S, send->base,
-                                       send->stride, S, (size_t)R, cudaMemcpyDeviceToDevice, st));
+        // one 1-D copy per (sender q, destination r), sender-major: the R
+        // copies of a segment follow one another, so the engines read it from
+        // L2 after the first.  On GB300 this ran 1.8x faster than one 2-D
+        // copy per destination (rows = senders) and 1.4x faster than the
+        // destination-major order.
+        for (int q = 0; q < R; ++q)
+            for (int r = 0; r < R; ++r)
+                SYM_CUDA(cudaMemcpyAsync(recv->base + (size_t)r * recv->stride + (size_t)q * S,
+                                         send->base + (size_t)q * send->stride, S,
+                                         cudaMemcpyDeviceToDevice, st));
         return SYM_OK;
     }
     if (algo == SYM_ALGO_PUT_SIGNAL) {
@@ -559,37 +649,32 @@ sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtyp
     a.giveup = recv->giveup;
     a.timeout_ns = timeout_ns ? std::min(timeout_ns, (uint64_t)60000000000ull) : default_timeout_ns();
     const size_t pairs = (size_t)R * R;
-    const int occ = occupancy((const void*)k_alltoall, kPutThreads, 0);
-    const size_t cap = (size_t)occ * recv->ctx->num_sms;
-    size_t pieces;
-    if (signalled) {
-        // receivers wait in the same launch, so every block must be resident:
-        // about two parts per resident CTA, each >= 64 KiB
-        pieces = std::max<size_t>(1, ceil_div(2 * cap, pairs));
-        pieces = std::min(pieces, std::max<size_t>(1, a.B / (64 * 1024)));
-    } else {
-        // no waits: one 32 KiB part per block (one pass of block_copy), blocks
-        // started in index order as in the other streaming kernels
-        pieces = std::max<size_t>(1, ceil_div(a.B, (size_t)kPutThreads * kPutU * 16));
-    }
+    // parts of about 32 KiB (one pass of block_copy) for the copy form, one
+    // block each; about 256 KiB for the put + signal form, whose parts also
+    // count arrivals and take a ticket
+    const size_t part = signalled ? (256u << 10) : (size_t)kPutThreads * kPutU * 16;
+    const size_t pieces = std::max<size_t>(1, ceil_div(a.B, part));
     a.piece = ceil_div(a.B, pieces);
     if (a.vec) a.piece = ceil_div(a.piece, (size_t)16) * 16;
     a.pieces = (uint32_t)ceil_div(a.B, a.piece);
     const size_t items = pairs * a.pieces;
-    if (items > 0x7fffffffu) return SYM_ERR_UNSUPPORTED;
-    a.nproducers = (uint32_t)(signalled ? std::min(items, cap) : items);
+    if (items + R > 0x7fffffffu) return SYM_ERR_UNSUPPORTED;
     if (signalled) {
         a.sig = recv->sig;
         a.nsig = recv->nsignals;
         a.pair_done = recv->pair_arrivals;
-        k_reset_slot0<<<1, 64, 0, st>>>(a.sig, a.nsig, R, recv->epoch);
+        a.ticket = recv->ticket;
+        k_reset_slot0<<<1, 64, 0, st>>>(a.sig, a.nsig, R, recv->epoch, recv->ticket);
         count_launch();
+        const int occ = occupancy((const void*)k_alltoall, kPutThreads, 0);
+        const size_t grid = std::min(items + R, (size_t)occ * recv->ctx->num_sms);
         void* args[] = {&a};
-        // receivers wait on senders of the same launch -> co-residency required
-        SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_alltoall, dim3(a.nproducers),
+        // all blocks resident (cooperative launch); the ticket order alone
+        // already keeps every wait on parts that running blocks hold
+        SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_alltoall, dim3((unsigned)grid),
                                              dim3(kPutThreads), args, 0, st));
     } else {
-        k_alltoall<<<a.nproducers, kPutThreads, 0, st>>>(a);
+        k_alltoall<<<(unsigned)items, kPutThreads, 0, st>>>(a);
     }
     count_launch();
     SYM_CUDA(cudaGetLastError());

@@ -31,6 +31,7 @@ enum WaitSite : uint32_t {
     kSitePullFlag = 3,
     kSitePutSignalRecv = 4,
     kSiteBulkStage = 5,
+    kSiteSignalChain = 6,      // a put waited for the previous batch's signal of its pair
 };
 
 // Per-device context: the status block and the arrival ring used by
@@ -67,9 +68,11 @@ struct sym_window {
     uint32_t* flags;       // device [R][flag_tiles]: per-tile ready flags (epoch-tagged)
     uint32_t* arrivals;    // device [R][flag_tiles]: per-tile producer counters (zero when idle)
     uint32_t* pair_arrivals;  // device [R][R]: pieces done per (sender, receiver) (zero when idle)
+    uint32_t* pair_ring;      // device [R][R][2]: pieces of a batch done, by batch parity (zero when idle)
     size_t flag_tiles;     // flag slots per rank
     uint32_t* epoch;       // device word: epoch of the last waiting launch (bumped on device)
     uint32_t* giveup;      // device word: epoch of the last launch whose wait gave up
+    unsigned long long* ticket;   // device word: next work item of a flag-synchronised launch
     void* aux;             // the allocation holding sig, cnt and flags
     symar::DevCtx* ctx;
 };
@@ -103,7 +106,10 @@ bool allgather_use_bulk();        // env SYM_ALLGATHER_KERNEL=bulk (default)|lds
 // Grid waves between a tile's producing item and the items that wait for it
 // (flag-synchronised kernels); env SYM_PULL_LAG_WAVES, default 4, 1..64.
 uint32_t pull_lag_waves();
-uint32_t fused_lag_waves();       // the same for the fused producer; env SYM_FUSED_LAG_WAVES, default 3
+// Tile blocks between the producers and the consumers of a tile in the fused
+// producer + AllReduce; env SYM_FUSED_LAG_BLOCKS, -1 when unset (then about
+// one grid wave).
+int64_t fused_lag_blocks();
 // Fault injection for failure-detection tests (env SYM_TEST_DROP_LAST_SIGNAL=1):
 // the put + signal AllGather's (0 -> 0) stream omits its last signal, so its
 // receiver's bounded wait runs out.  Off by default; never needs a GPU fault.
@@ -139,6 +145,11 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
 
 __device__ __forceinline__ void red_release_add_u64(uint64_t* p, uint64_t v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Strong (relaxed, gpu scope) add; preceded by a fence it forms a release pattern.
+__device__ __forceinline__ void red_relaxed_add_u64(uint64_t* p, uint64_t v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
@@ -197,7 +208,23 @@ __device__ __forceinline__ bool bounded_spin(Pred pred, uint64_t timeout_ns,
 // launch (never to 0, the value of fresh flags), and the launch reads it at
 // start.  A launch recorded in a CUDA graph therefore gets a new epoch on
 // every replay.
-sym_status_t bump_epoch(uint32_t* epoch, cudaStream_t st);   // enqueues the bump
+// The bump also zeroes the window's item ticket (if given) for the launch.
+sym_status_t bump_epoch(uint32_t* epoch, cudaStream_t st, unsigned long long* ticket = nullptr);
+
+// Work items of a persistent, flag-synchronised launch are handed out in
+// index order by one atomic ticket, not by a static stride: the items in
+// flight then stay a compact range (HBM pages close together, like blocks
+// of a non-persistent grid), and an item that waits only ever waits for
+// items handed out before it, which running blocks already hold.  s_slot is
+// a __shared__ pair; every thread of the block must call this.
+__device__ __forceinline__ uint64_t fetch_item(unsigned long long* ticket, unsigned long long* s_slot,
+                                               int& par) {
+    if (threadIdx.x == 0) s_slot[par] = atomicAdd(ticket, 1ull);
+    __syncthreads();
+    const uint64_t w = s_slot[par];
+    par ^= 1;
+    return w;
+}
 
 __device__ __forceinline__ uint32_t read_epoch(const uint32_t* epoch) {
     __shared__ uint32_t s_epoch;

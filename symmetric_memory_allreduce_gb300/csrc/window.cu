@@ -100,10 +100,11 @@ bool twoshot_use_bulk() {
     return v;
 }
 
-uint32_t fused_lag_waves() {
-    static const uint32_t v = [] {
-        uint64_t w = env_u64("SYM_FUSED_LAG_WAVES", 3);
-        return (uint32_t)(w < 1 ? 1 : (w > 64 ? 64 : w));
+int64_t fused_lag_blocks() {
+    static const int64_t v = [] {
+        const uint64_t none = ~0ull;
+        uint64_t b = env_u64("SYM_FUSED_LAG_BLOCKS", none);
+        return b == none ? (int64_t)-1 : (int64_t)(b > 4096 ? 4096 : b);
     }();
     return v;
 }
@@ -168,13 +169,14 @@ DevCtx* dev_ctx(int device) {
     return c;
 }
 
-__global__ void k_bump_epoch(uint32_t* epoch) {
+__global__ void k_bump_epoch(uint32_t* epoch, unsigned long long* ticket) {
     uint32_t e = *epoch + 1u;
     *epoch = e ? e : 1u;
+    if (ticket) *ticket = 0ull;
 }
 
-sym_status_t bump_epoch(uint32_t* epoch, cudaStream_t st) {
-    k_bump_epoch<<<1, 1, 0, st>>>(epoch);
+sym_status_t bump_epoch(uint32_t* epoch, cudaStream_t st, unsigned long long* ticket) {
+    k_bump_epoch<<<1, 1, 0, st>>>(epoch, ticket);
     count_launch();
     SYM_CUDA(cudaGetLastError());
     return SYM_OK;
@@ -193,7 +195,9 @@ static sym_status_t alloc_aux(sym_window* w) {
     size_t cnt_b = sizeof(uint64_t) * (size_t)w->R * w->ncounters;
     size_t flg_b = sizeof(uint32_t) * (size_t)w->R * w->flag_tiles;
     size_t pair_b = sizeof(uint32_t) * (size_t)w->R * w->R;
-    size_t total = sig_b + cnt_b + 2 * flg_b + pair_b + 2 * sizeof(uint32_t);
+    size_t ring_b = 2 * pair_b;      // [R][R][2] per-stream batch arrival ring
+    // the item ticket (u64) leads, so every u64 array stays 8-byte aligned
+    size_t total = sizeof(uint64_t) + sig_b + cnt_b + 2 * flg_b + pair_b + ring_b + 2 * sizeof(uint32_t);
     char* p = nullptr;
     SYM_CUDA(cudaMalloc(&p, total));
     cudaError_t e = cudaMemset(p, 0, total);
@@ -202,12 +206,15 @@ static sym_status_t alloc_aux(sym_window* w) {
         return cuda_fail(e, "cudaMemset(window slots)");
     }
     w->aux = p;
+    w->ticket = (unsigned long long*)p;
+    p += sizeof(uint64_t);
     w->sig = (uint64_t*)p;
     w->cnt = (uint64_t*)(p + sig_b);
     w->flags = (uint32_t*)(p + sig_b + cnt_b);
     w->arrivals = (uint32_t*)(p + sig_b + cnt_b + flg_b);
     w->pair_arrivals = (uint32_t*)(p + sig_b + cnt_b + 2 * flg_b);
-    w->epoch = (uint32_t*)(p + sig_b + cnt_b + 2 * flg_b + pair_b);
+    w->pair_ring = (uint32_t*)(p + sig_b + cnt_b + 2 * flg_b + pair_b);
+    w->epoch = (uint32_t*)(p + sig_b + cnt_b + 2 * flg_b + pair_b + ring_b);
     w->giveup = w->epoch + 1;
     return SYM_OK;
 }
