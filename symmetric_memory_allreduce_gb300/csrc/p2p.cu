@@ -20,6 +20,8 @@
 
 namespace symar {
 
+bool put_use_bulk();              // env SYM_PUT_KERNEL=bulk (default) | ldst (window.cu)
+
 constexpr int kCopyThreads = 256;
 constexpr int kCopyU = 4;
 constexpr int kPutThreads = 512;
@@ -163,6 +165,7 @@ struct PsArgs {
     uint32_t* giveup;         // recv window give-up word
     uint64_t timeout_ns;
     int vec;
+    int bulk;                 // puts by bulk copies (needs vec); else register copies
     int drop_last_signal;     // fault injection for tests: pair (0 -> 0) omits its last signal
 };
 
@@ -177,6 +180,50 @@ __device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* s_red) {
         for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += s_red[i];
     __syncthreads();
     return t;
+}
+
+// Bulk copy (TMA engine) of [lo, hi) from src to dst by one thread, through a
+// ring of kPsStages 16 KiB shared-memory stages: loads run kPsStages - 1 tiles
+// ahead of the stores.  `gtile` counts the tiles this block has moved so far
+// (it carries the mbarrier phases from one call to the next).  Returns when
+// every store has completed, or false if a stage's load did not arrive within
+// the bound.  lo, hi, src and dst are 16-byte aligned.
+constexpr int kPsStages = 4;
+constexpr uint32_t kPsTile = 16384;
+constexpr size_t kPsSmem = (size_t)kPsStages * kPsTile + kPsStages * sizeof(uint64_t);
+
+__device__ __forceinline__ bool bulk_copy_range(const char* src, char* dst, size_t lo, size_t hi,
+                                                unsigned char* stage, uint64_t* full, uint32_t& gtile) {
+    const uint32_t n = (uint32_t)((hi - lo + kPsTile - 1) / kPsTile);
+    auto bytes_of = [&](uint32_t i) { return (uint32_t)min((size_t)kPsTile, hi - lo - (size_t)i * kPsTile); };
+    auto load = [&](uint32_t i) {
+        const uint32_t s = (gtile + i) % kPsStages;
+        mbar_expect_tx(&full[s], bytes_of(i));
+        bulk_load(stage + (size_t)s * kPsTile, src + lo + (size_t)i * kPsTile, bytes_of(i), &full[s]);
+    };
+    for (uint32_t i = 0; i + 1 < (uint32_t)kPsStages && i < n; ++i) load(i);
+    bool ok = true;
+    for (uint32_t i = 0; i < n && ok; ++i) {
+        const uint32_t g = gtile + i, s = g % kPsStages;
+        uint32_t spins = 0;
+        while (!mbar_try_wait(&full[s], (g / kPsStages) & 1u))
+            if (++spins > (1u << 26)) {                   // bounded: loads of valid ranges arrive
+                ok = false;
+                break;
+            }
+        if (!ok) break;
+        bulk_store(dst + lo + (size_t)i * kPsTile, stage + (size_t)s * kPsTile, bytes_of(i));
+        bulk_commit();
+        const uint32_t nxt = i + kPsStages - 1;           // refills the stage of tile i-1
+        if (nxt < n) {
+            bulk_wait_read<1>();
+            load(nxt);
+        }
+    }
+    bulk_wait_all<0>();                                   // the stores are complete
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // ... and ordered before generic accesses
+    gtile += n;
+    return ok;
 }
 
 // Work items are handed out in index order by the window's ticket
@@ -200,7 +247,15 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
     __shared__ unsigned long long s_item[2];
     __shared__ int s_ok[2];
     __shared__ uint64_t s_red[kPutThreads / 32];
-    const uint32_t tag = read_epoch(a.epoch);      // bumped by the reset kernel before
+    extern __shared__ __align__(128) unsigned char ps_stage[];   // a.bulk: kPsSmem bytes
+    uint64_t* ps_full = reinterpret_cast<uint64_t*>(ps_stage + (size_t)kPsStages * kPsTile);
+    uint32_t gtile = 0;
+    bool copy_ok = true;
+    if (a.bulk && threadIdx.x == 0) {
+        for (int i = 0; i < kPsStages; ++i) mbar_init(&ps_full[i], 1);
+        fence_mbar_init();
+    }
+    const uint32_t tag = read_epoch(a.epoch);      // bumped by the reset kernel before (syncs the block)
     const uint32_t R = (uint32_t)a.R, pairs = R * R;
     const uint64_t puts = (uint64_t)pairs * a.ppi;
     const uint64_t row = puts + (a.mismatch ? pairs : 0u);
@@ -216,7 +271,9 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
         const uint32_t b0 = r * a.bpr, b1 = min(b0 + a.bpr, a.nbatches);
         if (r < a.nrows && slot < puts) {
             // ---- a put item: stream (q -> p), piece j
-            // streams vary fastest: the items in flight cover one piece of many streams
+            // streams vary fastest (the items in flight cover one piece of many
+            // streams), senders fastest within them (peer-major measured 1-3 %
+            // faster than sender-major)
             const uint32_t j = (uint32_t)(slot / pairs), pr = (uint32_t)(slot - (uint64_t)j * pairs);
             const uint32_t p = pr / R, q = pr - p * R;
             uint32_t k0, k1;                      // chunks
@@ -230,15 +287,23 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
             const char* src = a.send + (size_t)q * a.sstride;
             char* dst = a.recv + (size_t)p * a.rstride + (size_t)q * a.S;
             const size_t lo = min((size_t)k0 * a.chunk, a.S), hi = min((size_t)k1 * a.chunk, a.S);
-            block_copy<kPutThreads, kPutU>(src, dst, lo, hi, a.vec != 0);
+            if (a.bulk) {
+                if (threadIdx.x == 0 && hi > lo)
+                    copy_ok = bulk_copy_range(src, dst, lo, hi, ps_stage, ps_full, gtile);
+            } else {
+                block_copy<kPutThreads, kPutU>(src, dst, lo, hi, a.vec != 0);
+            }
             __syncthreads();
             if (threadIdx.x == 0) {
                 __threadfence();
-                if (k1 > k0)
+                if (!copy_ok)      // no signal: the stream's receiver then reports as well
+                    report_timeout(a.status, a.giveup, tag, kSiteBulkStage, (uint32_t)(w >> 32),
+                                   (uint32_t)w);
+                if (copy_ok && k1 > k0)
                     atomicAdd(reinterpret_cast<unsigned long long*>(a.cnt + (size_t)q * a.ncnt),
                               (unsigned long long)(k1 - k0));          // local completion
                 uint64_t* sp = sig_at(p, q);
-                bool last = true, ok = true;
+                bool last = true, ok = copy_ok;
                 if (a.ppi > 1) {
                     // free ring entry: batch b0-2 signalled
                     const uint64_t need = b0 >= 2 ? b0 - 1 : 0;
@@ -494,6 +559,7 @@ static sym_status_t launch_put_signal_allgather(sym_win_t send, sym_win_t recv, 
     a.timeout_ns = timeout_ns ? timeout_ns : default_timeout_ns();
     if (a.timeout_ns > 60000000000ull) a.timeout_ns = 60000000000ull;
     a.vec = (S % 16 == 0 && chunk % 16 == 0) ? 1 : 0;
+    a.bulk = a.vec && put_use_bulk() ? 1 : 0;
     a.drop_last_signal = test_drop_last_signal() ? 1 : 0;
     a.ticket = recv->ticket;
     a.ring = recv->pair_ring;
@@ -512,7 +578,14 @@ static sym_status_t launch_put_signal_allgather(sym_win_t send, sym_win_t recv, 
     }
     k_reset_slots<<<1, 256, 0, st>>>(a.sig, a.nsig, a.cnt, a.ncnt, R, recv->epoch, recv->ticket);
     count_launch();
-    const int occ = occupancy((const void*)k_put_signal_allgather, kPutThreads, 0);
+    const size_t smem = a.bulk ? kPsSmem : 0;
+    if (a.bulk)
+        SYM_CUDA(cudaFuncSetAttribute((const void*)k_put_signal_allgather,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPsSmem));
+    int occ = 0;
+    SYM_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, (const void*)k_put_signal_allgather,
+                                                           kPutThreads, smem));
+    if (occ < 1) return SYM_ERR_UNSUPPORTED;
     const size_t cap = (size_t)occ * recv->ctx->num_sms;
     const size_t pairs = (size_t)R * R;
     const size_t items = (pairs * a.ppi + (d_mismatch ? pairs : 0)) * a.nrows + (d_mismatch ? 0 : pairs);
@@ -521,7 +594,7 @@ static sym_status_t launch_put_signal_allgather(sym_win_t send, sym_win_t recv, 
     // all blocks resident (cooperative launch); the ticket order alone already
     // keeps every wait on items that running blocks hold
     SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_put_signal_allgather, dim3((unsigned)grid),
-                                         dim3(kPutThreads), args, 0, st));
+                                         dim3(kPutThreads), args, smem, st));
     count_launch();
     if (trace_on())
         fprintf(stderr, "[symar] put_signal_allgather R=%d S=%zu chunk=%zu B=%u grid=%zu items=%zu\n",

@@ -109,6 +109,14 @@ int64_t fused_lag_blocks() {
     return v;
 }
 
+bool put_use_bulk() {
+    static const bool v = [] {
+        const char* s = getenv("SYM_PUT_KERNEL");
+        return !(s && strcmp(s, "ldst") == 0);
+    }();
+    return v;
+}
+
 bool allgather_use_bulk() {
     static const bool v = [] {
         const char* s = getenv("SYM_ALLGATHER_KERNEL");
