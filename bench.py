@@ -504,19 +504,12 @@ def run_sweep(args) -> int:
             send.write(r, x[r])
         stream.synchronize()
         for algo in algos:
-            iters = max(5, min(2000, int(2e9 / max(nbytes * 2 * R, 1))))
-            for _ in range(5):
-                sm.sym_allreduce(send, recv, n, "f32", "sum", algo)
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(iters)]
-            torch.cuda.synchronize()
-            for s, e in ev:
-                s.record(stream)
-                sm.sym_allreduce(send, recv, n, "f32", "sum", algo)
-                e.record(stream)
-            torch.cuda.synchronize()
+            # >= 20 launches and >= 200 ms of timed launches, after 5 warm-ups
+            iters = max(20, min(2000, int(2e9 / max(nbytes * 2 * R, 1))))
+            ts = _time_launches(lambda: sm.sym_allreduce(send, recv, n, "f32", "sum", algo), iters,
+                                stream, None, 200.0)
+            iters = len(ts)
             assert sm.sym_stream_status() == sm.SYM_OK
-            ts = [s.elapsed_time(e) for s, e in ev]
             med = statistics.median(ts)
             comp = algo_bytes(algo, R, nbytes)["compulsory"]
             row = {"bytes_per_rank": nbytes, "algo": algo, "iters": iters,
@@ -554,26 +547,32 @@ def run_sweep(args) -> int:
     return 0
 
 
-def _time_launches(fn, iters: int, stream, flush=None) -> list[float]:
+def _time_launches(fn, iters: int, stream, flush=None, min_ms: float = 0.0) -> list[float]:
     """Per-launch CUDA-event times (ms) of fn() on `stream`, after 5 warm-ups.
 
-    flush: a device buffer larger than L2, overwritten before every timed
-    launch (outside its events) so that the launch starts with a cold L2."""
+    At least `iters` launches, repeated in batches of `iters` until the timed
+    launches add up to `min_ms`.  flush: a device buffer larger than L2,
+    overwritten before every timed launch (outside its events) so that the
+    launch starts with a cold L2."""
     import torch
 
     for _ in range(5):
         fn()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(iters)]
-    for s, e in ev:
-        if flush is not None:
-            flush.zero_()
-        s.record(stream)
-        fn()
-        e.record(stream)
-    torch.cuda.synchronize()
-    return [s.elapsed_time(e) for s, e in ev]
+    out: list[float] = []
+    while True:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(iters)]
+        for s, e in ev:
+            if flush is not None:
+                flush.zero_()
+            s.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        out += [s.elapsed_time(e) for s, e in ev]
+        if sum(out) >= min_ms or len(out) >= 100 * iters:
+            return out
 
 
 L2_FLUSH_BYTES = 256 << 20       # about twice the 126 MiB L2
@@ -624,6 +623,12 @@ def run_suite(args) -> int:
     def its(n):
         return args.suite_iters or n
 
+    # every row: >= 20 launches and >= 200 ms of timed launches (fixed count with --suite-iters)
+    min_ms = 0.0 if args.suite_iters else 200.0
+
+    def timed(fn, iters, stream_, flush=None):
+        return _time_launches(fn, iters, stream_, flush, min_ms)
+
     scale = max(1, args.scale)
     wanted = [w.strip() for w in args.rows.split(",") if w.strip()]
 
@@ -646,7 +651,7 @@ def run_suite(args) -> int:
             send.write(r, x[r])
         stream.synchronize()
         for algo in algos:
-            ts = _time_launches(lambda: sm.sym_allreduce(send, recv, n, dt, "sum", algo),
+            ts = timed(lambda: sm.sym_allreduce(send, recv, n, dt, "sum", algo),
                                 iters_for(2 * R * S), stream)
             m = algo_bytes(algo, R, S)
             resident = 2 * R * S < (126 << 20)
@@ -654,7 +659,7 @@ def run_suite(args) -> int:
                    {"R": R, "bytes_per_rank": S, "l2_resident": resident})
             if resident:
                 # the same launches with L2 flushed before each one (cold column)
-                ts = _time_launches(lambda: sm.sym_allreduce(send, recv, n, dt, "sum", algo),
+                ts = timed(lambda: sm.sym_allreduce(send, recv, n, dt, "sum", algo),
                                     its(50), stream, flush)
                 report(f"allreduce config{cfg}", f"{algo} {dt} cold L2", ts, S, m["compulsory"],
                        m["logical"], {"R": R, "bytes_per_rank": S, "l2_resident": False})
@@ -673,14 +678,14 @@ def run_suite(args) -> int:
         stream.synchronize()
         comp = R * S + R * R * S
         for algo in ("copy", "ce") if want("allgather") else ():
-            ts = _time_launches(lambda: sm.sym_allgather(send, recv, S // 4, "f32", algo), its(50),
+            ts = timed(lambda: sm.sym_allgather(send, recv, S // 4, "f32", algo), its(50),
                                 stream)
             kern = os.environ.get("SYM_ALLGATHER_KERNEL", "bulk") if algo == "copy" else "copy engines"
             report("allgather config5", algo, ts, S, comp,
                    extra={"R": R, "bytes_per_rank": S, "kernel": kern})
         nchunks = -(-S // cfg5["chunk"])
         for batch in (8, 1, 64) if want("put_signal") else ():
-            ts = _time_launches(lambda: sm.sym_allgather(send, recv, S // 4, "f32", "put_signal",
+            ts = timed(lambda: sm.sym_allgather(send, recv, S // 4, "f32", "put_signal",
                                                          cfg5["chunk"], batch), its(50), stream)
             report("put_signal allgather config5", f"chunk 64KiB, {batch} chunks/signal", ts, S, comp,
                    extra={"R": R, "bytes_per_rank": S, "signals_per_pair": -(-nchunks // batch)})
@@ -696,7 +701,7 @@ def run_suite(args) -> int:
             send.write(r, xa[r])
         stream.synchronize()
         for algo in ("copy", "put_signal"):
-            ts = _time_launches(lambda: sm.sym_alltoall(send, recv, B // 4, "f32", algo), its(100),
+            ts = timed(lambda: sm.sym_alltoall(send, recv, B // 4, "f32", algo), its(100),
                                 stream)
             report("alltoall", algo, ts, R * B, 2 * R * R * B, extra={"R": R, "bytes_per_segment": B})
         send.free()
@@ -712,7 +717,7 @@ def run_suite(args) -> int:
             win_in.write(r, x[r])
         stream.synchronize()
         alpha = [1.0 + 0.25 * r for r in range(R)]
-        ts = _time_launches(lambda: sm.sym_scale_allreduce(win_in, send, recv, alpha, n), its(100),
+        ts = timed(lambda: sm.sym_scale_allreduce(win_in, send, recv, alpha, n), its(100),
                             stream)
         report("fused producer + allreduce", "scale then two-shot, counter relay", ts, S,
                3 * R * S, extra={"R": R, "bytes_per_rank": S,
@@ -727,11 +732,11 @@ def run_suite(args) -> int:
         nb = (2 << 30) // scale
         src = torch.empty(nb // 4, dtype=torch.float32, device="cuda").normal_()
         dst = torch.empty_like(src)
-        ts = _time_launches(lambda: torch.mul(src, 1.0, out=dst), its(50), stream)
+        ts = timed(lambda: torch.mul(src, 1.0, out=dst), its(50), stream)
         report("ceiling", "SM copy (torch elementwise)", ts, nb, 2 * nb, extra={"bytes": nb})
-        ts = _time_launches(lambda: dst.copy_(src), its(50), stream)
+        ts = timed(lambda: dst.copy_(src), its(50), stream)
         report("ceiling", "device copy (torch copy_)", ts, nb, 2 * nb, extra={"bytes": nb})
-        ts = _time_launches(lambda: dst.fill_(1.0), its(50), stream)
+        ts = timed(lambda: dst.fill_(1.0), its(50), stream)
         report("ceiling", "write only (torch fill_)", ts, nb, nb, extra={"bytes": nb})
         del src, dst
     return 0
