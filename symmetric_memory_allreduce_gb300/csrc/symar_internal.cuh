@@ -104,7 +104,7 @@ size_t oneshot_max_bytes();
 bool twoshot_use_bulk();          // env SYM_TWOSHOT_KERNEL=bulk|ldst
 bool allgather_use_bulk();        // env SYM_ALLGATHER_KERNEL=bulk (default)|ldst
 // Grid waves between a tile's producing item and the items that wait for it
-// (flag-synchronised kernels); env SYM_PULL_LAG_WAVES, default 4, 1..64.
+// (fused pull two-shot); env SYM_PULL_LAG_WAVES, default 4, 1..64.
 uint32_t pull_lag_waves();
 // Tile blocks between the producers and the consumers of a tile in the fused
 // producer + AllReduce; env SYM_FUSED_LAG_BLOCKS, -1 when unset (then about

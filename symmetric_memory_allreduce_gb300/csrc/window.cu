@@ -81,7 +81,7 @@ size_t oneshot_max_bytes() {
 
 uint32_t pull_lag_waves() {
     static const uint32_t v = [] {
-        uint64_t w = env_u64("SYM_PULL_LAG_WAVES", 8);
+        uint64_t w = env_u64("SYM_PULL_LAG_WAVES", 4);
         return (uint32_t)(w < 1 ? 1 : (w > 64 ? 64 : w));
     }();
     return v;
