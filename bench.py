@@ -401,7 +401,7 @@ def run_ours(args) -> int:
         "config": _config(R, n, args.algo),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "k_twoshot_st<F32T,8,2>" if args.algo in ("twoshot", "auto")
+                     "kernel": "k_twoshot_st<F32T,8,1>" if args.algo in ("twoshot", "auto")
                      else args.algo, "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "bytes_per_launch": bytes_model["compulsory"],
                      "kernel_ms": kern_ms, "kernel_ms_p10": percentile(per, 0.1),
@@ -524,7 +524,7 @@ def run_sweep(args) -> int:
                 cold = _time_launches(lambda: sm.sym_allreduce(send, recv, n, "f32", "sum", algo),
                                       min(iters, 50), stream, flush)
                 row["us_median_cold"] = statistics.median(cold) * 1e3
-            if nbytes <= (1 << 20):
+            if nbytes <= (16 << 20):
                 # device-side latency: 100 calls recorded in a CUDA graph, replayed
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):

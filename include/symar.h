@@ -140,7 +140,7 @@ sym_status_t sym_window_read(sym_win_t w, int rank, size_t off, void* dst, size_
  * count: elements per rank; count*sizeof(dtype) <= bytes of both windows.
  * send == recv (in place) is allowed for the two-shot algorithms, not for
  * ONESHOT.  count == 0 is a no-op.  AUTO picks ONESHOT up to
- * SYM_ONESHOT_MAX_BYTES per rank (env, default 256 KiB), else TWOSHOT.
+ * SYM_ONESHOT_MAX_BYTES per rank (env, default 128 KiB), else TWOSHOT.
  * TWOSHOT_PULL enqueues a one-thread kernel that advances the recv window's
  * flag epoch on the device before the main launch, so the call can be
  * recorded into a CUDA graph and replayed; every algorithm only enqueues

@@ -74,8 +74,9 @@ uint64_t default_timeout_ns() {
 
 size_t oneshot_max_bytes() {
     // measured crossover on GB300 (R = 8, device time per call from CUDA-graph
-    // replay): one-shot is faster up to 256 KiB per rank, two-shot from 1 MiB
-    static const size_t v = (size_t)env_u64("SYM_ONESHOT_MAX_BYTES", 262144);
+    // replay): one-shot is faster up to 64 KiB per rank, two-shot from 256 KiB;
+    // the default splits the gap (geometric mean)
+    static const size_t v = (size_t)env_u64("SYM_ONESHOT_MAX_BYTES", 131072);
     return v;
 }
 
