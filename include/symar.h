@@ -223,9 +223,11 @@ sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym
  * (expected 0).  Requires recv nsignals >= R, send ncounters >= 1.
  * If one receiver's wait runs out, the launch's other waits stop early (each
  * launch is tagged with the recv window's device epoch).  For failure tests,
- * env SYM_TEST_DROP_LAST_SIGNAL=1 makes the (0 -> 0) stream omit its last
- * signal, so that receiver's wait runs out (read once per process; off by
- * default).
+ * env SYM_TEST_DROP_SIGNAL=last (or SYM_TEST_DROP_LAST_SIGNAL=1) makes the
+ * (0 -> 0) stream omit its last signal, so that receiver's wait runs out
+ * (site 4); SYM_TEST_DROP_SIGNAL=first makes it omit its first signal, so the
+ * stream's next batch runs out waiting to signal in order (site 6).  Read once
+ * per process; off by default.
  * Errors: INVALID_ARG, CUDA; a wait that runs out -> SYM_ERR_TIMEOUT from
  * sym_stream_status(). */
 sym_status_t sym_allgather_put_signal(sym_win_t send, sym_win_t recv, size_t bytes_per_rank,

@@ -166,7 +166,7 @@ struct PsArgs {
     uint64_t timeout_ns;
     int vec;
     int bulk;                 // puts by bulk copies (needs vec); else register copies
-    int drop_last_signal;     // fault injection for tests: pair (0 -> 0) omits its last signal
+    int drop_signal;          // fault injection for tests: stream (0 -> 0) omits its last (1) or first (2) signal
 };
 
 __device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* s_red) {
@@ -326,7 +326,8 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
                     // batches' bytes and the acquired predecessor; one add per batch
                     if (ok) __threadfence();
                     for (uint32_t b = b0; ok && b < b1; ++b) {
-                        const bool dropped = a.drop_last_signal && pr == 0 && b + 1 == a.nbatches;
+                        const bool dropped = pr == 0 && ((a.drop_signal == 1 && b + 1 == a.nbatches) ||
+                                                         (a.drop_signal == 2 && b == 0));
                         if (!dropped) red_relaxed_add_u64(sp, 1ull);
                     }
                 }
@@ -560,7 +561,7 @@ static sym_status_t launch_put_signal_allgather(sym_win_t send, sym_win_t recv, 
     if (a.timeout_ns > 60000000000ull) a.timeout_ns = 60000000000ull;
     a.vec = (S % 16 == 0 && chunk % 16 == 0) ? 1 : 0;
     a.bulk = a.vec && put_use_bulk() ? 1 : 0;
-    a.drop_last_signal = test_drop_last_signal() ? 1 : 0;
+    a.drop_signal = test_drop_signal();
     a.ticket = recv->ticket;
     a.ring = recv->pair_ring;
     // about 512 KiB per item: whole batches when a batch is at most that

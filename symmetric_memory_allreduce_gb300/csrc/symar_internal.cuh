@@ -110,10 +110,13 @@ uint32_t pull_lag_waves();
 // producer + AllReduce; env SYM_FUSED_LAG_BLOCKS, -1 when unset (then about
 // one grid wave).
 int64_t fused_lag_blocks();
-// Fault injection for failure-detection tests (env SYM_TEST_DROP_LAST_SIGNAL=1):
-// the put + signal AllGather's (0 -> 0) stream omits its last signal, so its
-// receiver's bounded wait runs out.  Off by default; never needs a GPU fault.
-bool test_drop_last_signal();
+// Fault injection for failure-detection tests: the put + signal AllGather's
+// (0 -> 0) stream omits one signal, so a bounded wait runs out.  1 = its last
+// signal (env SYM_TEST_DROP_SIGNAL=last, or SYM_TEST_DROP_LAST_SIGNAL=1): the
+// stream's receiver waits; 2 = its first signal (SYM_TEST_DROP_SIGNAL=first):
+// the stream's next batch waits to signal in order.  0 (default) = off.
+// Never needs a GPU fault.
+int test_drop_signal();
 int occupancy(const void* kernel, int threads, size_t smem);   // blocks per SM, cached
 size_t dtype_size(sym_dtype_t t);       // 0 if unknown
 

@@ -88,8 +88,13 @@ uint32_t pull_lag_waves() {
     return v;
 }
 
-bool test_drop_last_signal() {
-    static const bool v = env_u64("SYM_TEST_DROP_LAST_SIGNAL", 0) != 0;
+int test_drop_signal() {
+    static const int v = [] {
+        const char* s = getenv("SYM_TEST_DROP_SIGNAL");
+        if (s && strcmp(s, "first") == 0) return 2;
+        if (s && strcmp(s, "last") == 0) return 1;
+        return env_u64("SYM_TEST_DROP_LAST_SIGNAL", 0) != 0 ? 1 : 0;
+    }();
     return v;
 }
 

@@ -59,3 +59,53 @@ def test_dropped_signal_times_out_cleanly():
     assert out.returncode == 0, out.stdout[-3000:] + out.stderr[-3000:]
     assert "FAILURE_TEST_OK" in out.stdout
     assert "site 4" in out.stdout          # the put + signal receiver reported it
+
+
+_SCRIPT_FIRST = r"""
+import sys, time
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import numpy as np
+import oracle
+import symmetric_memory_allreduce_gb300 as sm
+from _gpu_util import upload, download
+sm.load(); oracle.build()
+# one batch (8 chunks) per work item, and enough items (8 streams x 16 batches)
+# that the receivers start well after the stream's second batch begins to wait
+R, S, chunk, B = 8, 8 << 20, 65536, 8
+x = np.random.default_rng(10).integers(0, 256, size=(R, S), dtype=np.uint8)
+send, recv = sm.Window(R, S, ncounters=1), sm.Window(R, R * S, nsignals=R)
+upload(send, x)
+t0 = time.time()
+sm.sym_allgather_put_signal(send, recv, S, chunk, B, timeout_ns=50_000_000)
+st = sm.sym_stream_status()
+dt = time.time() - t0
+print("STATUS", sm.sym_status_string(st), "SECONDS", round(dt, 3), "WHERE", sm.sym_last_error())
+assert st == sm.SYM_ERR_TIMEOUT, st
+assert dt < 10.0
+# batch 0 of (0 -> 0) never signalled, so no later batch of that stream may signal
+assert sm.sym_signal_read(recv, 0, 0) == 0
+# the bytes all arrived (the copies do not wait; only the signals are ordered)
+assert np.array_equal(download(recv, R * S, ranks=[0])[0], oracle.allgather(x))
+# the context stays usable
+y = np.random.default_rng(2).standard_normal((R, 1000)).astype(np.float32)
+a, b = sm.Window(R, 4000), sm.Window(R, 4000)
+upload(a, y)
+sm.sym_allreduce(a, b, 1000, "f32", "sum", "twoshot_pull")
+assert sm.sym_stream_status() == sm.SYM_OK
+got = download(b, 4000, np.float32)
+assert np.array_equal(got[0].view(np.uint32), oracle.allreduce_sum_f32(y).view(np.uint32))
+print("FAILURE_TEST_OK")
+"""
+
+
+def test_dropped_first_signal_stops_the_stream_in_order():
+    """The (0 -> 0) stream omits its first signal (SYM_TEST_DROP_SIGNAL=first):
+    the put of its second batch waits for it to keep the signals in batch order,
+    runs out (site 6), and no later signal of the stream is added."""
+    env = dict(os.environ, SYM_TEST_DROP_SIGNAL="first")
+    out = subprocess.run([sys.executable, "-c", _SCRIPT_FIRST.format(root=ROOT,
+                                                                     tests=os.path.join(ROOT, "tests"))],
+                         env=env, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stdout[-3000:] + out.stderr[-3000:]
+    assert "FAILURE_TEST_OK" in out.stdout
+    assert "site 6" in out.stdout          # the batch-order wait reported it
