@@ -752,7 +752,8 @@ def parse(argv=None):
                     choices=["auto", "oneshot", "twoshot", "twoshot_pull", "twoshot_split"])
     ap.add_argument("--ranks", type=int, default=R_DEFAULT)
     ap.add_argument("--count", type=int, default=N_DEFAULT)
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=40,
+                    help="end-to-end steps (the pipeline's fill and drain amortise over them)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
