@@ -20,8 +20,6 @@
 
 namespace symar {
 
-bool put_use_bulk();              // env SYM_PUT_KERNEL=bulk (default) | ldst (window.cu)
-
 constexpr int kCopyThreads = 256;
 constexpr int kCopyU = 4;
 constexpr int kPutThreads = 512;
