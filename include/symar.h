@@ -213,8 +213,9 @@ sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym
  * Batches of different (q, p) streams run in parallel; the signals of one
  * stream are added in batch order (the put of batch k waits, bounded, until
  * the stream's signal reads k).  When S and chunk_bytes are multiples of 16
- * the bytes move by bulk copies through shared memory (TMA engine; env
- * SYM_PUT_KERNEL=ldst selects register copies), else by register copies.
+ * the bytes move by bulk copies through shared memory (TMA engine), the R
+ * puts of one source range of a sender sharing one read; env
+ * SYM_PUT_KERNEL=ldst selects register copies per stream, as do other sizes.
  * The same launch holds the receivers: each (p, q) waits (bounded by
  * timeout_ns, 0 = default) until its signal reaches that count.
  * If d_mismatch (device pointer to one uint64) is not NULL, receivers check

@@ -180,17 +180,20 @@ __device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* s_red) {
     return t;
 }
 
-// Bulk copy (TMA engine) of [lo, hi) from src to dst by one thread, through a
-// ring of kPsStages 16 KiB shared-memory stages: loads run kPsStages - 1 tiles
-// ahead of the stores.  `gtile` counts the tiles this block has moved so far
-// (it carries the mbarrier phases from one call to the next).  Returns when
-// every store has completed, or false if a stage's load did not arrive within
-// the bound.  lo, hi, src and dst are 16-byte aligned.
+// Bulk copy (TMA engine) of [lo, hi) from src to ndst destinations (dst,
+// dst + dst_stride, ...) by one thread, through a ring of kPsStages 16 KiB
+// shared-memory stages: each tile is loaded once and stored ndst times; loads
+// run kPsStages - 1 tiles ahead of the stores.  `gtile` counts the tiles this
+// block has moved so far (it carries the mbarrier phases from one call to the
+// next).  Returns when every store has completed, or false if a stage's load
+// did not arrive within the bound.  lo, hi, src, dst and dst_stride are
+// 16-byte aligned.
 constexpr int kPsStages = 4;
 constexpr uint32_t kPsTile = 16384;
 constexpr size_t kPsSmem = (size_t)kPsStages * kPsTile + kPsStages * sizeof(uint64_t);
 
-__device__ __forceinline__ bool bulk_copy_range(const char* src, char* dst, size_t lo, size_t hi,
+__device__ __forceinline__ bool bulk_copy_range(const char* src, char* dst, size_t dst_stride,
+                                                uint32_t ndst, size_t lo, size_t hi,
                                                 unsigned char* stage, uint64_t* full, uint32_t& gtile) {
     const uint32_t n = (uint32_t)((hi - lo + kPsTile - 1) / kPsTile);
     auto bytes_of = [&](uint32_t i) { return (uint32_t)min((size_t)kPsTile, hi - lo - (size_t)i * kPsTile); };
@@ -210,7 +213,9 @@ __device__ __forceinline__ bool bulk_copy_range(const char* src, char* dst, size
                 break;
             }
         if (!ok) break;
-        bulk_store(dst + lo + (size_t)i * kPsTile, stage + (size_t)s * kPsTile, bytes_of(i));
+        for (uint32_t d = 0; d < ndst; ++d)
+            bulk_store(dst + (size_t)d * dst_stride + lo + (size_t)i * kPsTile,
+                       stage + (size_t)s * kPsTile, bytes_of(i));
         bulk_commit();
         const uint32_t nxt = i + kPsStages - 1;           // refills the stage of tile i-1
         if (nxt < n) {
@@ -225,25 +230,28 @@ __device__ __forceinline__ bool bulk_copy_range(const char* src, char* dst, size
 }
 
 // Work items are handed out in index order by the window's ticket
-// (fetch_item) and move about 512 KiB each, whatever the batch size: in a row
-// of items, every (q -> p) stream has either one item that puts `bpr` whole
-// batches (small batches), or `ppi` items that each put a piece of one batch
-// (large batches).  With the prefix check on, each row ends with one check
-// item per stream; with it off, one receiver item per stream follows the last
-// row and waits for the final count.
+// (fetch_item) and have a fixed size whatever the batch size: in a row of
+// items, either one item puts `bpr` whole batches (small batches) or `ppi`
+// items each put a piece of one batch (large batches).  With bulk copies an
+// item is 128 KiB of sender q's source put to all R peers (the R puts of the
+// same range share one read, as the SM AllGather does); with register copies
+// it is 512 KiB of one (q -> p) stream.  With the prefix check on, each row
+// ends with one check item per stream; with it off, one receiver item per
+// stream follows the last row and waits for the final count.
 //
 // A batch's signal must follow the previous batch's signal of the same
 // stream: the item that completes batch b first waits (acquire) until the
 // stream's signal reads b, then adds 1 with a release, so a receiver that
 // reads k sees batches 0..k-1 (each release carries the earlier ones by
 // causality).  Pieces of a batch count their arrivals in a two-entry ring per
-// stream (by batch parity); a piece of batch b first waits until batch b-2 is
-// signalled, which frees its ring entry.  Every wait is for items handed out
+// stream, or per sender with bulk copies (by batch parity); a piece of batch b
+// first waits until batch b-2 is signalled, which frees its ring entry.  Every wait is for items handed out
 // earlier, which running blocks hold, so no wait depends on a block that has
 // not started.
 __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) {
     __shared__ unsigned long long s_item[2];
     __shared__ int s_ok[2];
+    __shared__ int s_sig;             // the put item completes a batch: add its signals
     __shared__ uint64_t s_red[kPutThreads / 32];
     extern __shared__ __align__(128) unsigned char ps_stage[];   // a.bulk: kPsSmem bytes
     uint64_t* ps_full = reinterpret_cast<uint64_t*>(ps_stage + (size_t)kPsStages * kPsTile);
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
     }
     const uint32_t tag = read_epoch(a.epoch);      // bumped by the reset kernel before (syncs the block)
     const uint32_t R = (uint32_t)a.R, pairs = R * R;
-    const uint64_t puts = (uint64_t)pairs * a.ppi;
+    const uint64_t puts = (uint64_t)(a.bulk ? R : pairs) * a.ppi;
     const uint64_t row = puts + (a.mismatch ? pairs : 0u);
     const uint64_t total = row * a.nrows + (a.mismatch ? 0ull : (uint64_t)pairs);
     int ipar = 0, opar = 0;
@@ -268,12 +276,27 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
         // batches [b0, b1) of this row
         const uint32_t b0 = r * a.bpr, b1 = min(b0 + a.bpr, a.nbatches);
         if (r < a.nrows && slot < puts) {
-            // ---- a put item: stream (q -> p), piece j
-            // streams vary fastest (the items in flight cover one piece of many
-            // streams), senders fastest within them (peer-major measured 1-3 %
-            // faster than sender-major)
-            const uint32_t j = (uint32_t)(slot / pairs), pr = (uint32_t)(slot - (uint64_t)j * pairs);
-            const uint32_t p = pr / R, q = pr - p * R;
+            // ---- a put item: piece j of the row for one stream (q -> p), or,
+            // with bulk copies, for all R streams of sender q at once (the R
+            // puts of the same source range read it once)
+            uint32_t q, p0, np, j, key;
+            if (a.bulk) {
+                j = (uint32_t)(slot / R);
+                q = (uint32_t)(slot - (uint64_t)j * R);
+                p0 = 0;
+                np = R;
+                key = q;
+            } else {
+                // streams vary fastest (the items in flight cover one piece of
+                // many streams), senders fastest within them (peer-major
+                // measured 1-3 % faster than sender-major)
+                j = (uint32_t)(slot / pairs);
+                const uint32_t pr = (uint32_t)(slot - (uint64_t)j * pairs);
+                p0 = pr / R;
+                q = pr - p0 * R;
+                np = 1;
+                key = pr;
+            }
             uint32_t k0, k1;                      // chunks
             if (a.ppi == 1) {
                 k0 = b0 * a.B;
@@ -283,11 +306,11 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
                 k1 = min(min(k0 + a.gchunks, (b0 + 1) * a.B), a.nchunks);
             }
             const char* src = a.send + (size_t)q * a.sstride;
-            char* dst = a.recv + (size_t)p * a.rstride + (size_t)q * a.S;
+            char* dst = a.recv + (size_t)p0 * a.rstride + (size_t)q * a.S;
             const size_t lo = min((size_t)k0 * a.chunk, a.S), hi = min((size_t)k1 * a.chunk, a.S);
             if (a.bulk) {
                 if (threadIdx.x == 0 && hi > lo)
-                    copy_ok = bulk_copy_range(src, dst, lo, hi, ps_stage, ps_full, gtile);
+                    copy_ok = bulk_copy_range(src, dst, a.rstride, np, lo, hi, ps_stage, ps_full, gtile);
             } else {
                 block_copy<kPutThreads, kPutU>(src, dst, lo, hi, a.vec != 0);
             }
@@ -299,16 +322,18 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
                                    (uint32_t)w);
                 if (copy_ok && k1 > k0)
                     atomicAdd(reinterpret_cast<unsigned long long*>(a.cnt + (size_t)q * a.ncnt),
-                              (unsigned long long)(k1 - k0));          // local completion
-                uint64_t* sp = sig_at(p, q);
+                              (unsigned long long)(k1 - k0) * np);      // local completion
                 bool last = true, ok = copy_ok;
-                if (a.ppi > 1) {
-                    // free ring entry: batch b0-2 signalled
+                if (a.ppi > 1 && ok) {
+                    // free ring entry: batch b0-2 signalled (its last piece
+                    // reset the entry before adding any of its signals)
                     const uint64_t need = b0 >= 2 ? b0 - 1 : 0;
+                    const uint64_t* sp = sig_at(p0, q);
                     ok = need == 0 || bounded_spin([&] { return ld_acquire_u64(sp) >= need; },
                                                    a.timeout_ns, a.giveup, tag);
+                    if (!ok) report_timeout(a.status, a.giveup, tag, kSiteSignalChain, p0, q);
                     if (ok) {
-                        uint32_t* cnt = a.ring + ((size_t)pr << 1) + (b0 & 1u);
+                        uint32_t* cnt = a.ring + ((size_t)key << 1) + (b0 & 1u);
                         last = atomicAdd(cnt, 1u) == a.ppi - 1;
                         if (last) {
                             *cnt = 0;
@@ -316,20 +341,33 @@ __global__ void __launch_bounds__(kPutThreads) k_put_signal_allgather(PsArgs a) 
                         }
                     }
                 }
-                if (ok && last) {
+                s_sig = ok && last ? 1 : 0;
+            }
+            __syncthreads();
+            if (s_sig) {
+                // batch order: thread i waits (acquire) until stream (p0 + i -> q)
+                // has signalled batch b0-1, then, once all have, adds that
+                // stream's signals for batches b0..b1-1 after a fence (a release
+                // pattern: it carries the item's bytes, ordered before the
+                // barrier, and the acquired predecessor)
+                bool okp = true;
+                const uint32_t p = p0 + threadIdx.x;
+                if (threadIdx.x < np && b0 > 0) {
+                    const uint64_t* sp = sig_at(p, q);
                     const uint64_t before = b0;
-                    ok = b0 == 0 || bounded_spin([&] { return ld_acquire_u64(sp) >= before; },
-                                                 a.timeout_ns, a.giveup, tag);
-                    // one release pattern (fence, then strong adds) covers the
-                    // batches' bytes and the acquired predecessor; one add per batch
-                    if (ok) __threadfence();
-                    for (uint32_t b = b0; ok && b < b1; ++b) {
-                        const bool dropped = pr == 0 && ((a.drop_signal == 1 && b + 1 == a.nbatches) ||
-                                                         (a.drop_signal == 2 && b == 0));
-                        if (!dropped) red_relaxed_add_u64(sp, 1ull);
+                    okp = bounded_spin([&] { return ld_acquire_u64(sp) >= before; }, a.timeout_ns,
+                                       a.giveup, tag);
+                    if (!okp) report_timeout(a.status, a.giveup, tag, kSiteSignalChain, p, q);
+                }
+                if (__syncthreads_and(okp) && threadIdx.x < np) {
+                    __threadfence();
+                    for (uint32_t b = b0; b < b1; ++b) {
+                        const bool dropped = p == 0 && q == 0 &&
+                                             ((a.drop_signal == 1 && b + 1 == a.nbatches) ||
+                                              (a.drop_signal == 2 && b == 0));
+                        if (!dropped) red_relaxed_add_u64(sig_at(p, q), 1ull);
                     }
                 }
-                if (!ok) report_timeout(a.status, a.giveup, tag, kSiteSignalChain, p, q);
             }
         } else if (r < a.nrows) {
             // ---- check: once the signal shows batch b1-1, batches [b0, b1) equal the source
@@ -562,8 +600,10 @@ static sym_status_t launch_put_signal_allgather(sym_win_t send, sym_win_t recv, 
     a.drop_signal = test_drop_signal();
     a.ticket = recv->ticket;
     a.ring = recv->pair_ring;
-    // about 512 KiB per item: whole batches when a batch is at most that
-    const size_t gch = std::max<size_t>(1, (512 * 1024) / chunk);
+    // per item: about 512 KiB of one stream (register copies), or 128 KiB of
+    // a sender's source written to all R peers (bulk copies); whole batches
+    // when a batch is at most that
+    const size_t gch = std::max<size_t>(1, (a.bulk ? 128 * 1024 : 512 * 1024) / chunk);
     if (B <= gch) {
         a.bpr = (uint32_t)std::max<size_t>(1, gch / B);
         a.ppi = 1;
@@ -587,7 +627,8 @@ static sym_status_t launch_put_signal_allgather(sym_win_t send, sym_win_t recv, 
     if (occ < 1) return SYM_ERR_UNSUPPORTED;
     const size_t cap = (size_t)occ * recv->ctx->num_sms;
     const size_t pairs = (size_t)R * R;
-    const size_t items = (pairs * a.ppi + (d_mismatch ? pairs : 0)) * a.nrows + (d_mismatch ? 0 : pairs);
+    const size_t items = ((a.bulk ? (size_t)R : pairs) * a.ppi + (d_mismatch ? pairs : 0)) * a.nrows +
+                         (d_mismatch ? 0 : pairs);
     const size_t grid = std::max<size_t>(1, std::min(items, cap));
     void* args[] = {&a};
     // all blocks resident (cooperative launch); the ticket order alone already
