@@ -133,8 +133,9 @@ sym_status_t sym_window_read(sym_win_t w, int rank, size_t off, void* dst, size_
  *   recv_r[i] = ((send_0[i] + send_1[i]) + ...) + send_{R-1}[i]   for all r,
  * added in rank order 0..R-1 (so fp32 results are bit-exact and identical on
  * every rank).  bf16 / fp16 inputs are widened exactly, accumulated in fp32
- * and rounded to nearest-even once.  SYM_MAX / SYM_MIN take the IEEE maxNum /
- * minNum of the same values.
+ * and rounded to nearest-even once.  SYM_MAX / SYM_MIN fold the same values
+ * with IEEE 754-2019 maximumNumber / minimumNumber (a NaN operand is ignored;
+ * -0 < +0).
  * [SYMEX] Example 1: ncclAllReduce(send, recv, count, float, sum, comm,
  * stream) on symmetric windows; each element is the sum over all ranks.
  * count: elements per rank; count*sizeof(dtype) <= bytes of both windows.
