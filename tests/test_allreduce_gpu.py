@@ -286,7 +286,7 @@ def test_config3_full_f32(symar, oracle):
     """R=8 x 67,108,864 fp32 U(-1,1) (256 MiB per rank), two-shot forms."""
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
-    _full(symar, oracle, wl.config_inputs(3), "f32", ["twoshot", "twoshot_pull", "auto"])
+    _full(symar, oracle, wl.config_inputs(3), "f32", ["twoshot", "twoshot_pull", "twoshot_split", "auto"])
 
 
 def test_config3_full_bf16(symar, oracle):
@@ -294,7 +294,7 @@ def test_config3_full_bf16(symar, oracle):
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
     xb = wl.to_bf16_bits(wl.config_inputs(3))
-    _full(symar, oracle, xb, "bf16", ["twoshot", "twoshot_pull"])
+    _full(symar, oracle, xb, "bf16", ["twoshot", "twoshot_pull", "twoshot_split"])
 
 
 @pytest.mark.parametrize("nbytes", [1024 * 4 ** k for k in range(10)])
