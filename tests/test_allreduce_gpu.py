@@ -297,6 +297,30 @@ def test_config3_full_bf16(symar, oracle):
     _full(symar, oracle, xb, "bf16", ["twoshot", "twoshot_pull", "twoshot_split"])
 
 
+def test_config3_full_f16(symar, oracle):
+    """The same draws rounded to fp16 (128 MiB per rank): fp32 accumulation in rank
+    order, one rounding, bit-exact on every rank for the two-shot forms."""
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    x = np.ascontiguousarray(wl.config_inputs(3).astype(np.float16).view(np.uint16))
+    R, n = x.shape
+    want = oracle.allreduce(x, "f16", "sum")
+    send, recv = symar.Window(R, n * 2), symar.Window(R, n * 2)
+    try:
+        upload(send, x)
+        for algo in ["twoshot", "twoshot_pull", "twoshot_split"]:
+            symar.sym_allreduce(send, recv, n, "f16", "sum", algo)
+            assert symar.sym_stream_status() == symar.SYM_OK
+            for r in (0, R // 2, R - 1):
+                y = download(recv, n * 2, np.uint16, ranks=[r])[0]
+                assert np.array_equal(y, want), (algo, r)
+            recv.tensor().zero_()
+            sync()
+    finally:
+        send.free()
+        recv.free()
+
+
 @pytest.mark.parametrize("nbytes", [1024 * 4 ** k for k in range(10)])
 def test_config4_sweep(symar, oracle, nbytes):
     """R=8, 1 KiB .. 256 MiB per rank, fp32 N(0,1), every algorithm and AUTO."""
