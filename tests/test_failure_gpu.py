@@ -69,9 +69,10 @@ import oracle
 import symmetric_memory_allreduce_gb300 as sm
 from _gpu_util import upload, download
 sm.load(); oracle.build()
-# one batch (8 chunks) per work item, and enough items (8 streams x 16 batches)
-# that the receivers start well after the stream's second batch begins to wait
-R, S, chunk, B = 8, 8 << 20, 65536, 8
+# enough work items (8 senders x 64 batches of 8 chunks) that the receivers,
+# which come after every put, start long after the stream's second batch
+# begins to wait for the missing first signal
+R, S, chunk, B = 8, 32 << 20, 65536, 8
 x = np.random.default_rng(10).integers(0, 256, size=(R, S), dtype=np.uint8)
 send, recv = sm.Window(R, S, ncounters=1), sm.Window(R, R * S, nsignals=R)
 upload(send, x)
