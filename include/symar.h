@@ -82,7 +82,7 @@ typedef enum {
     /* AllGather */
     SYM_ALGO_COPY = 5,           /* read each segment once, store it to all R ranks */
     SYM_ALGO_PUT_SIGNAL = 6,     /* chunked puts, one strong signal per batch, receivers wait */
-    SYM_ALGO_CE = 7              /* copy engines, no kernel: one 2-D memcpy per destination */
+    SYM_ALGO_CE = 7              /* copy engines, no kernel: one 1-D memcpy per (sender, destination) */
 } sym_algo_t;
 
 /* ---------------------------------------------------------------- windows */
@@ -96,6 +96,31 @@ typedef enum {
  * Errors: INVALID_ARG, OOM, CUDA.  On error *out is set to NULL. */
 sym_status_t sym_window_alloc(int R, size_t bytes_per_rank, uint32_t nsignals,
                               uint32_t ncounters, sym_win_t* out);
+
+/* How a window's memory was obtained (sym_window_kind). */
+typedef enum {
+    SYM_WINDOW_CUDA_MALLOC = 0,       /* one cudaMalloc of R*stride bytes */
+    SYM_WINDOW_REGISTERED = 1,        /* caller memory (sym_window_register) */
+    SYM_WINDOW_VMM_EXPORTABLE = 2,    /* VMM, one physical allocation per rank, POSIX-fd handles */
+    SYM_WINDOW_VMM = 3                /* VMM, one physical allocation per rank, no exportable handle */
+} sym_window_kind_t;
+
+/* The same windows from the virtual-memory API, as [SYMEX]'s symmetric
+ * allocator builds them: one physical allocation per rank (cuMemCreate,
+ * with a POSIX-file-descriptor handle where the platform allows one), all
+ * mapped back to back into one reserved virtual range (cuMemAddressReserve,
+ * cuMemMap) with read-write access for the device (cuMemSetAccess).  The
+ * layout is the one above -- rank r at base + r*stride -- with stride rounded
+ * up to the allocation granularity (2 MiB on GB300), so every collective
+ * works on these windows unchanged.  Falls back to one cudaMalloc, as the
+ * allocator on the pages does, when the platform has no VMM support;
+ * sym_window_kind() tells which.  Errors: INVALID_ARG, CUDA.  On error *out
+ * is NULL. */
+sym_status_t sym_window_alloc_vmm(int R, size_t bytes_per_rank, uint32_t nsignals,
+                                  uint32_t ncounters, sym_win_t* out);
+
+/* sym_window_kind_t of a window; -1 for NULL. */
+int sym_window_kind(sym_win_t w);
 
 /* Wrap caller-owned device memory (e.g. a torch tensor) as R windows at
  * base + r*stride.  base must be 256-byte aligned, stride a multiple of 4096

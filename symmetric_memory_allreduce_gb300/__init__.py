@@ -12,5 +12,6 @@ from ._binding import (  # noqa: F401
     sym_allreduce_noalloc, sym_signal, sym_signal_read, sym_signal_reset, sym_signal_wait,
     sym_status_string,
     sym_stream_status,
+    SYM_WINDOW_CUDA_MALLOC, SYM_WINDOW_REGISTERED, SYM_WINDOW_VMM, SYM_WINDOW_VMM_EXPORTABLE,
 )
 from ._binding import LIB_PATH  # noqa: F401

@@ -25,6 +25,7 @@ SYM_SUM, SYM_MAX, SYM_MIN = 0, 1, 2
 SYM_ALGO_AUTO, SYM_ALGO_ONESHOT, SYM_ALGO_TWOSHOT = 0, 1, 2
 SYM_ALGO_TWOSHOT_PULL, SYM_ALGO_TWOSHOT_SPLIT = 3, 4
 SYM_ALGO_COPY, SYM_ALGO_PUT_SIGNAL, SYM_ALGO_CE = 5, 6, 7
+SYM_WINDOW_CUDA_MALLOC, SYM_WINDOW_REGISTERED, SYM_WINDOW_VMM_EXPORTABLE, SYM_WINDOW_VMM = 0, 1, 2, 3
 NO_ID = 0xFFFFFFFF
 
 ALGOS = {"auto": SYM_ALGO_AUTO, "oneshot": SYM_ALGO_ONESHOT, "twoshot": SYM_ALGO_TWOSHOT,
@@ -48,6 +49,8 @@ P, sz, i32, u32, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_
 PP = ctypes.POINTER(ctypes.c_void_p)
 _SIGS = {
     "sym_window_alloc": ([i32, sz, u32, u32, PP], i32),
+    "sym_window_alloc_vmm": ([i32, sz, u32, u32, PP], i32),
+    "sym_window_kind": ([P], i32),
     "sym_window_register": ([P, i32, sz, sz, u32, u32, PP], i32),
     "sym_window_free": ([P], i32),
     "sym_window_rank_ptr": ([P, i32, PP], i32),
@@ -127,13 +130,18 @@ def _handle(w):
 
 
 class Window:
-    """R equal rank windows in one device allocation (sym_window_alloc / sym_window_register)."""
+    """R equal rank windows (sym_window_alloc, sym_window_alloc_vmm with vmm=True, or
+    sym_window_register with base=...)."""
 
     def __init__(self, R: int, bytes_per_rank: int, nsignals: int = 0, ncounters: int = 0,
-                 base: int | None = None, stride: int | None = None, keepalive=None):
+                 base: int | None = None, stride: int | None = None, keepalive=None,
+                 vmm: bool = False):
         lib = load()
         h = ctypes.c_void_p()
-        if base is None:
+        if base is None and vmm:
+            _check(lib.sym_window_alloc_vmm(R, bytes_per_rank, nsignals, ncounters, ctypes.byref(h)),
+                   "sym_window_alloc_vmm")
+        elif base is None:
             _check(lib.sym_window_alloc(R, bytes_per_rank, nsignals, ncounters, ctypes.byref(h)),
                    "sym_window_alloc")
         else:
@@ -145,6 +153,7 @@ class Window:
         self.stride = lib.sym_window_stride(self.handle)
         self.device = lib.sym_window_device(self.handle)
         self.nsignals, self.ncounters = nsignals, ncounters
+        self.kind = lib.sym_window_kind(self.handle)
         self._keepalive = keepalive
 
     def rank_ptr(self, r: int) -> int:

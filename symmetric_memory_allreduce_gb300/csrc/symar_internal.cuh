@@ -75,6 +75,8 @@ struct sym_window {
     unsigned long long* ticket;   // device word: next work item of a flag-synchronised launch
     void* aux;             // the allocation holding sig, cnt and flags
     symar::DevCtx* ctx;
+    int kind;              // SYM_WINDOW_* : how base was allocated
+    unsigned long long* vmm_handles;   // VMM windows: one physical allocation per rank
 };
 
 namespace symar {

@@ -15,6 +15,9 @@
 #include <map>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "symar_internal.cuh"
 
 namespace symar {
@@ -233,8 +236,129 @@ static sym_status_t alloc_aux(sym_window* w) {
     return SYM_OK;
 }
 
+// ----------------------------------------------------------------- VMM windows
+//
+// [SYMEX] memory allocation: the symmetric allocator creates physical memory
+// with cuMemCreate (an exportable handle where the platform allows),
+// reserves a virtual range with cuMemAddressReserve, maps the memory there
+// with cuMemMap and grants access with cuMemSetAccess, and falls back to
+// cudaMalloc.  Here each rank's window is its own physical allocation, mapped
+// at base + r*stride of one reserved range, so the kernels' base + r*stride
+// addressing is unchanged.  The driver calls are looked up through the
+// runtime (cudaGetDriverEntryPointByVersion): the library does not link the
+// driver library itself.
+struct VmmApi {
+    PFN_cuMemGetAllocationGranularity_v10020 granularity = nullptr;
+    PFN_cuMemCreate_v10020 create = nullptr;
+    PFN_cuMemRelease_v10020 release = nullptr;
+    PFN_cuMemAddressReserve_v10020 reserve = nullptr;
+    PFN_cuMemAddressFree_v10020 addr_free = nullptr;
+    PFN_cuMemMap_v10020 map = nullptr;
+    PFN_cuMemUnmap_v10020 unmap = nullptr;
+    PFN_cuMemSetAccess_v10020 set_access = nullptr;
+    bool ok = false;
+};
+
+static const VmmApi& vmm_api() {
+    static const VmmApi api = [] {
+        VmmApi a;
+        auto get = [](const char* name, void** fn) {
+            cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+            return cudaGetDriverEntryPointByVersion(name, fn, 12000, cudaEnableDefault, &q) ==
+                       cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess && *fn != nullptr;
+        };
+        a.ok = get("cuMemGetAllocationGranularity", (void**)&a.granularity) &&
+               get("cuMemCreate", (void**)&a.create) && get("cuMemRelease", (void**)&a.release) &&
+               get("cuMemAddressReserve", (void**)&a.reserve) &&
+               get("cuMemAddressFree", (void**)&a.addr_free) && get("cuMemMap", (void**)&a.map) &&
+               get("cuMemUnmap", (void**)&a.unmap) && get("cuMemSetAccess", (void**)&a.set_access);
+        return a;
+    }();
+    return api;
+}
+
+// Undo a (possibly partial) VMM window: unmap and release `mapped` ranks,
+// then free the reserved range.
+static void vmm_release(char* base, size_t stride, int R, const unsigned long long* h, int mapped) {
+    const VmmApi& v = vmm_api();
+    for (int r = 0; r < mapped; ++r) {
+        v.unmap((CUdeviceptr)(base + (size_t)r * stride), stride);
+        v.release((CUmemGenericAllocationHandle)h[r]);
+    }
+    if (base) v.addr_free((CUdeviceptr)base, stride * (size_t)R);
+}
+
+// R physical allocations of `stride` bytes mapped back to back; kind reports
+// whether the memory carries an exportable (POSIX file descriptor) handle.
+static sym_status_t vmm_alloc(int dev, int R, size_t stride, char** base_out,
+                              unsigned long long** handles_out, int* kind_out) {
+    const VmmApi& v = vmm_api();
+    if (!v.ok) return SYM_ERR_UNSUPPORTED;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        CUmemAllocationProp prop = {};
+        prop.type = CU_MEM_ALLOCATION_TYPE_PINNED;
+        prop.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+        prop.location.id = dev;
+        prop.requestedHandleTypes =
+            attempt == 0 ? CU_MEM_HANDLE_TYPE_POSIX_FILE_DESCRIPTOR : CU_MEM_HANDLE_TYPE_NONE;
+        size_t gran = 0;
+        if (v.granularity(&gran, &prop, CU_MEM_ALLOC_GRANULARITY_MINIMUM) != CUDA_SUCCESS || !gran ||
+            stride % gran != 0)
+            continue;
+        CUdeviceptr base = 0;
+        if (v.reserve(&base, stride * (size_t)R, gran, 0, 0) != CUDA_SUCCESS) continue;
+        unsigned long long* h = new unsigned long long[R]();
+        int mapped = 0;
+        bool ok = true;
+        for (int r = 0; r < R && ok; ++r) {
+            CUmemGenericAllocationHandle hr = 0;
+            if (v.create(&hr, stride, &prop, 0) != CUDA_SUCCESS) {
+                ok = false;
+                break;
+            }
+            if (v.map(base + (CUdeviceptr)((size_t)r * stride), stride, 0, hr, 0) != CUDA_SUCCESS) {
+                v.release(hr);
+                ok = false;
+                break;
+            }
+            h[r] = (unsigned long long)hr;
+            ++mapped;
+        }
+        if (ok) {
+            CUmemAccessDesc acc = {};
+            acc.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+            acc.location.id = dev;
+            acc.flags = CU_MEM_ACCESS_FLAGS_PROT_READWRITE;
+            ok = v.set_access(base, stride * (size_t)R, &acc, 1) == CUDA_SUCCESS;
+        }
+        if (!ok) {
+            vmm_release((char*)base, stride, R, h, mapped);
+            delete[] h;
+            continue;
+        }
+        *base_out = (char*)base;
+        *handles_out = h;
+        *kind_out = attempt == 0 ? SYM_WINDOW_VMM_EXPORTABLE : SYM_WINDOW_VMM;
+        return SYM_OK;
+    }
+    return SYM_ERR_UNSUPPORTED;
+}
+
+static size_t vmm_granularity(int dev) {
+    const VmmApi& v = vmm_api();
+    if (!v.ok) return 0;
+    CUmemAllocationProp prop = {};
+    prop.type = CU_MEM_ALLOCATION_TYPE_PINNED;
+    prop.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+    prop.location.id = dev;
+    size_t gran = 0;
+    if (v.granularity(&gran, &prop, CU_MEM_ALLOC_GRANULARITY_MINIMUM) != CUDA_SUCCESS) return 0;
+    return gran;
+}
+
 static sym_status_t make_window(void* base, bool owns, int R, size_t bytes, size_t stride,
-                                uint32_t nsig, uint32_t ncnt, sym_win_t* out) {
+                                uint32_t nsig, uint32_t ncnt, sym_win_t* out, bool vmm = false) {
     int dev = 0;
     SYM_CUDA(cudaGetDevice(&dev));
     DevCtx* ctx = dev_ctx(dev);
@@ -249,7 +373,15 @@ static sym_status_t make_window(void* base, bool owns, int R, size_t bytes, size
     w->ncounters = ncnt;
     w->ctx = ctx;
     w->aux = nullptr;
-    if (owns) {
+    w->kind = owns ? SYM_WINDOW_CUDA_MALLOC : SYM_WINDOW_REGISTERED;
+    w->vmm_handles = nullptr;
+    if (owns && vmm) {
+        // the VMM path; a platform without it falls back to cudaMalloc below
+        char* p = nullptr;
+        if (vmm_alloc(dev, R, stride, &p, &w->vmm_handles, &w->kind) == SYM_OK) w->base = p;
+        else vmm = false;
+    }
+    if (owns && !vmm) {
         char* p = nullptr;
         cudaError_t e = cudaMalloc(&p, stride * (size_t)R);
         if (e != cudaSuccess) {
@@ -257,12 +389,18 @@ static sym_status_t make_window(void* base, bool owns, int R, size_t bytes, size
             return cuda_fail(e, "cudaMalloc(window)");
         }
         w->base = p;
-    } else {
+        w->kind = SYM_WINDOW_CUDA_MALLOC;
+    } else if (!owns) {
         w->base = (char*)base;
     }
     sym_status_t s = alloc_aux(w);
     if (s != SYM_OK) {
-        if (owns) cudaFree(w->base);
+        if (w->vmm_handles) {
+            vmm_release(w->base, w->stride, w->R, w->vmm_handles, w->R);
+            delete[] w->vmm_handles;
+        } else if (owns) {
+            cudaFree(w->base);
+        }
         delete w;
         return s;
     }
@@ -282,6 +420,24 @@ sym_status_t sym_window_alloc(int R, size_t bytes_per_rank, uint32_t nsignals, u
     size_t stride = ceil_div(bytes_per_rank, kWindowAlign) * kWindowAlign;
     return make_window(nullptr, true, R, bytes_per_rank, stride, nsignals, ncounters, out);
 }
+
+sym_status_t sym_window_alloc_vmm(int R, size_t bytes_per_rank, uint32_t nsignals,
+                                  uint32_t ncounters, sym_win_t* out) {
+    if (!out) return SYM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (R < 1 || R > kMaxRanks || bytes_per_rank == 0) return SYM_ERR_INVALID_ARG;
+    if (nsignals > (1u << 20) || ncounters > (1u << 20)) return SYM_ERR_INVALID_ARG;
+    if (bytes_per_rank > ((size_t)1 << 40)) return SYM_ERR_INVALID_ARG;
+    int dev = 0;
+    SYM_CUDA(cudaGetDevice(&dev));
+    size_t align = kWindowAlign;
+    const size_t gran = vmm_granularity(dev);
+    if (gran > align && gran % kWindowAlign == 0) align = gran;   // whole physical pages per rank
+    const size_t stride = ceil_div(bytes_per_rank, align) * align;
+    return make_window(nullptr, true, R, bytes_per_rank, stride, nsignals, ncounters, out, true);
+}
+
+int sym_window_kind(sym_win_t w) { return w ? w->kind : -1; }
 
 sym_status_t sym_window_register(void* base, int R, size_t bytes_per_rank, size_t stride,
                                  uint32_t nsignals, uint32_t ncounters, sym_win_t* out) {
@@ -307,7 +463,12 @@ sym_status_t sym_window_free(sym_win_t w) {
     DeviceGuard g(w->device);
     cudaError_t e = cudaDeviceSynchronize();
     if (w->aux) cudaFree(w->aux);
-    if (w->owns_base && w->base) cudaFree(w->base);
+    if (w->vmm_handles) {
+        vmm_release(w->base, w->stride, w->R, w->vmm_handles, w->R);
+        delete[] w->vmm_handles;
+    } else if (w->owns_base && w->base) {
+        cudaFree(w->base);
+    }
     delete w;
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize(window_free)");
     return SYM_OK;
