@@ -308,6 +308,19 @@ sym_status_t sym_put_signal(sym_win_t src, sym_win_t dst, int src_rank, int peer
                             size_t src_off, size_t bytes, uint32_t signal_id, uint32_t counter_id,
                             sym_stream_t stream);
 
+/* get: the one-sided read, the reverse of put.  Copies `bytes` from rank
+ * `peer`'s part of `remote` at remote_off into rank `rank`'s part of `local`
+ * at local_off.  [GIN] get(team, peer, remoteWnd, remoteOffset, localWnd,
+ * localOffset, bytes, ...): no remote action; the page's flush() is what
+ * makes the data visible to the reader, and on one GPU the stream order does
+ * that.  For in-kernel consumers, counter_id != UINT32_MAX adds 1 to counter
+ * slot counter_id of rank `rank` in `local` once every byte has landed
+ * (UINT32_MAX = none).  peer may equal rank (loopback) when the ranges do
+ * not overlap.  Ranges must lie inside the windows.  bytes == 0 with no
+ * counter is a no-op.  Errors: INVALID_ARG, CUDA. */
+sym_status_t sym_get(sym_win_t remote, sym_win_t local, int rank, int peer, size_t local_off,
+                     size_t remote_off, size_t bytes, uint32_t counter_id, sym_stream_t stream);
+
 /* Signal without data: add `value` to signal slot signal_id of rank `peer`
  * ([GIN] signal() with a SignalAdd action), with release ordering. */
 sym_status_t sym_signal(sym_win_t dst, int peer, uint32_t signal_id, uint64_t value,

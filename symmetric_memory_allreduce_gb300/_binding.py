@@ -65,6 +65,7 @@ _SIGS = {
     "sym_allgather": ([P, P, sz, i32, i32, sz, u32, P], i32),
     "sym_allgather_put_signal": ([P, P, sz, sz, u32, P, u64, P], i32),
     "sym_put_signal": ([P, P, i32, i32, sz, sz, sz, u32, u32, P], i32),
+    "sym_get": ([P, P, i32, i32, sz, sz, sz, u32, P], i32),
     "sym_alltoall": ([P, P, sz, i32, i32, u64, P], i32),
     "sym_scale_allreduce": ([P, P, P, P, sz, P], i32),
     "sym_allreduce_noalloc": ([P, P, sz, i32, sz, i32, i32, P], i32),
@@ -278,6 +279,12 @@ def sym_put_signal(src, dst, src_rank: int, peer: int, dst_off: int, src_off: in
                    signal_id: int = NO_ID, counter_id: int = NO_ID, stream=None):
     _check(_lib.sym_put_signal(_handle(src), _handle(dst), src_rank, peer, dst_off, src_off, nbytes,
                                signal_id, counter_id, _stream(stream)), "sym_put_signal")
+
+
+def sym_get(remote, local, rank: int, peer: int, local_off: int, remote_off: int, nbytes: int,
+            counter_id: int = NO_ID, stream=None):
+    _check(_lib.sym_get(_handle(remote), _handle(local), rank, peer, local_off, remote_off, nbytes,
+                        counter_id, _stream(stream)), "sym_get")
 
 
 def sym_signal(dst, peer: int, signal_id: int, value: int = 1, stream=None):

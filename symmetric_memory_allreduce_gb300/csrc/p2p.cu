@@ -795,6 +795,40 @@ sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtyp
     return SYM_OK;
 }
 
+sym_status_t sym_get(sym_win_t remote, sym_win_t local, int rank, int peer, size_t local_off,
+                     size_t remote_off, size_t bytes, uint32_t counter_id, sym_stream_t stream) {
+    if (!remote || !local || remote->device != local->device) return SYM_ERR_INVALID_ARG;
+    if (rank < 0 || rank >= local->R || peer < 0 || peer >= remote->R) return SYM_ERR_INVALID_ARG;
+    if (remote_off > remote->bytes || bytes > remote->bytes - remote_off) return SYM_ERR_INVALID_ARG;
+    if (local_off > local->bytes || bytes > local->bytes - local_off) return SYM_ERR_INVALID_ARG;
+    if (counter_id != UINT32_MAX && counter_id >= local->ncounters) return SYM_ERR_INVALID_ARG;
+    const char* s = remote->base + (size_t)peer * remote->stride + remote_off;
+    char* d = local->base + (size_t)rank * local->stride + local_off;
+    if (bytes && s < d + bytes && d < s + bytes) return SYM_ERR_INVALID_ARG;   // overlap
+    if (bytes == 0 && counter_id == UINT32_MAX) return SYM_OK;
+    DeviceGuard g(local->device);
+    if (!g.ok) return SYM_ERR_CUDA;
+    DevCtx* ctx = local->ctx;
+    // the put kernel with the roles turned round: the reader's window receives,
+    // and the local action lands on the reader's counter
+    PutArgs a{};
+    a.src = s;
+    a.dst = d;
+    a.bytes = bytes;
+    a.vec = ((((uintptr_t)s | (uintptr_t)d | bytes) & 15u) == 0) ? 1 : 0;
+    a.sig = nullptr;
+    a.cnt = counter_id != UINT32_MAX ? local->cnt + (size_t)rank * local->ncounters + counter_id
+                                     : nullptr;
+    a.arrive = ctx->arrive + (ctx->arrive_next++ % kArriveRing);
+    const size_t per_cta = 64 * 1024;
+    const size_t grid = std::max((size_t)1, std::min(ceil_div(bytes, per_cta),
+                                                     (size_t)ctx->num_sms * 4));
+    k_put<<<(unsigned)grid, kPutThreads, 0, (cudaStream_t)stream>>>(a);
+    count_launch();
+    SYM_CUDA(cudaGetLastError());
+    return SYM_OK;
+}
+
 sym_status_t sym_put_signal(sym_win_t src, sym_win_t dst, int src_rank, int peer, size_t dst_off,
                             size_t src_off, size_t bytes, uint32_t signal_id, uint32_t counter_id,
                             sym_stream_t stream) {

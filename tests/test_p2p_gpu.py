@@ -284,3 +284,39 @@ def test_alltoall_random(symar, oracle, R, B):
     finally:
         send.free()
         recv.free()
+
+
+def test_get_reads_peer_into_local(symar, oracle):
+    """[GIN] get: rank `rank` reads peer's bytes into its own window; the optional
+    local counter counts completed gets; loopback and argument checks."""
+    R, S = 4, 300_000 + 16
+    x = np.random.default_rng(61).integers(0, 256, size=(R, S), dtype=np.uint8)
+    remote, local = symar.Window(R, S), symar.Window(R, 2 * S, ncounters=2)
+    try:
+        upload(remote, x)
+        local.tensor().zero_()
+        # rank 1 gets peer 3's bytes 1000.. into its window at offset 16 (vector path)
+        symar.sym_get(remote, local, 1, 3, 16, 1008, 200_000, counter_id=1)
+        # rank 2 gets peer 0's bytes at odd offsets (byte path)
+        symar.sym_get(remote, local, 2, 0, S + 3, 5, 77_777, counter_id=1)
+        # loopback: rank 0 reads its own part of `local`, non-overlapping ranges
+        symar.sym_get(local, local, 0, 0, S, 0, 1000)
+        assert symar.sym_stream_status() == symar.SYM_OK
+        got = download(local, 2 * S)
+        assert np.array_equal(got[1, 16:16 + 200_000], x[3, 1008:1008 + 200_000])
+        assert np.array_equal(got[2, S + 3:S + 3 + 77_777], x[0, 5:5 + 77_777])
+        assert not got[1, :16].any() and not got[1, 16 + 200_000:].any()
+        assert symar.sym_counter_read(local, 1, 1) == 1
+        assert symar.sym_counter_read(local, 2, 1) == 1
+        assert symar.sym_counter_read(local, 0, 1) == 0
+        with pytest.raises(symar.SymError):
+            symar.sym_get(remote, local, 0, 4, 0, 0, 16)          # peer out of range
+        with pytest.raises(symar.SymError):
+            symar.sym_get(remote, local, 0, 0, 0, S - 8, 16)      # past the remote window
+        with pytest.raises(symar.SymError):
+            symar.sym_get(local, local, 0, 0, 0, 8, 64)           # overlapping loopback
+        with pytest.raises(symar.SymError):
+            symar.sym_get(remote, local, 0, 0, 0, 0, 16, counter_id=2)   # no such counter
+    finally:
+        remote.free()
+        local.free()
