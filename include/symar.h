@@ -37,7 +37,7 @@
  *    as SYM_ERR_TIMEOUT from sym_stream_status(); sym_last_error() then names
  *    the wait site: 1 signal wait, 2 counter wait, 3 pull-tile flag, 4 put +
  *    signal / AlltoAll receiver, 5 bulk-copy stage, 6 put + signal batch
- *    order.  No call traps the GPU.
+ *    order, 7 barrier.  No call traps the GPU.
  *  - Windows are owned by the library (sym_window_alloc) or by the caller
  *    (sym_window_register).  Free a window only after every stream that used
  *    it has finished with it; windows must be freed before unloading.
@@ -320,6 +320,18 @@ sym_status_t sym_put_signal(sym_win_t src, sym_win_t dst, int src_rank, int peer
  * counter is a no-op.  Errors: INVALID_ARG, CUDA. */
 sym_status_t sym_get(sym_win_t remote, sym_win_t local, int rank, int peer, size_t local_off,
                      size_t remote_off, size_t bytes, uint32_t counter_id, sym_stream_t stream);
+
+/* Barrier across the R rank slots of `w` on signal slot signal_id.  [GIN]
+ * ncclGinBarrierSession::sync with the strongest fence (Put | Get): every
+ * rank adds 1 to that slot of every rank with a release, then waits
+ * (acquire, bounded by timeout_ns, 0 = default) until its own slot has
+ * received all R adds, so work enqueued after the barrier sees everything
+ * every rank did before it.  Each barrier adds exactly R to every rank's
+ * slot; the slot must be used by nothing else.  A barrier that runs out
+ * (SYM_ERR_TIMEOUT, site 7) leaves the slots short: reset them
+ * (sym_signal_reset on every rank) before the next barrier.  One cooperative
+ * launch of R blocks.  Errors: INVALID_ARG, CUDA. */
+sym_status_t sym_barrier(sym_win_t w, uint32_t signal_id, uint64_t timeout_ns, sym_stream_t stream);
 
 /* Signal without data: add `value` to signal slot signal_id of rank `peer`
  * ([GIN] signal() with a SignalAdd action), with release ordering. */

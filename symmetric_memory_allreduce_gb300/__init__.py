@@ -7,7 +7,7 @@ in include/symar.h); this package is its thin ctypes binding.
 from ._binding import (  # noqa: F401
     ALGOS, DTYPES, NO_ID, OPS, SYM_ERR_INVALID_ARG, SYM_ERR_TIMEOUT, SYM_ERR_UNSUPPORTED, SYM_OK,
     SymError, Window, header_symbols, load, sym_abi_version, sym_allgather,
-    sym_allgather_put_signal, sym_allreduce, sym_alltoall, sym_scale_allreduce, sym_allreduce_algo, sym_counter_read,
+    sym_allgather_put_signal, sym_allreduce, sym_alltoall, sym_barrier, sym_scale_allreduce, sym_allreduce_algo, sym_counter_read,
     sym_counter_reset, sym_counter_wait, sym_get, sym_last_error, sym_launch_count, sym_put_signal,
     sym_allreduce_noalloc, sym_signal, sym_signal_read, sym_signal_reset, sym_signal_wait,
     sym_status_string,

@@ -66,6 +66,7 @@ _SIGS = {
     "sym_allgather_put_signal": ([P, P, sz, sz, u32, P, u64, P], i32),
     "sym_put_signal": ([P, P, i32, i32, sz, sz, sz, u32, u32, P], i32),
     "sym_get": ([P, P, i32, i32, sz, sz, sz, u32, P], i32),
+    "sym_barrier": ([P, u32, u64, P], i32),
     "sym_alltoall": ([P, P, sz, i32, i32, u64, P], i32),
     "sym_scale_allreduce": ([P, P, P, P, sz, P], i32),
     "sym_allreduce_noalloc": ([P, P, sz, i32, sz, i32, i32, P], i32),
@@ -285,6 +286,10 @@ def sym_get(remote, local, rank: int, peer: int, local_off: int, remote_off: int
             counter_id: int = NO_ID, stream=None):
     _check(_lib.sym_get(_handle(remote), _handle(local), rank, peer, local_off, remote_off, nbytes,
                         counter_id, _stream(stream)), "sym_get")
+
+
+def sym_barrier(w, signal_id: int = 0, timeout_ns: int = 0, stream=None):
+    _check(_lib.sym_barrier(_handle(w), signal_id, timeout_ns, _stream(stream)), "sym_barrier")
 
 
 def sym_signal(dst, peer: int, signal_id: int, value: int = 1, stream=None):

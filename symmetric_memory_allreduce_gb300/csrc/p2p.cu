@@ -862,6 +862,48 @@ sym_status_t sym_put_signal(sym_win_t src, sym_win_t dst, int src_rank, int peer
     return SYM_OK;
 }
 
+// [GIN] ncclGinBarrierSession::sync, signal form: one block per rank r reads
+// its slot (before adding anything), adds 1 to slot `id` of every rank with a
+// release, then waits (acquire, bounded) until its own slot has gained all R
+// adds of this barrier.  Each barrier adds exactly R to every slot, so the
+// target is the next multiple of R above the value read first.
+__global__ void __launch_bounds__(kMaxRanks) k_barrier(uint64_t* sig, uint32_t nsig, uint32_t id,
+                                                       int R, uint64_t timeout_ns, uint32_t* status) {
+    __shared__ uint64_t s_target;
+    const uint32_t r = blockIdx.x;
+    uint64_t* mine = sig + (size_t)r * nsig + id;
+    if (threadIdx.x == 0) s_target = (ld_acquire_u64(mine) / (uint64_t)R + 1) * (uint64_t)R;
+    __syncthreads();
+    if (threadIdx.x < (uint32_t)R) {
+        __threadfence();
+        red_release_add_u64(sig + (size_t)threadIdx.x * nsig + id, 1ull);
+    }
+    if (threadIdx.x == 0) {
+        const uint64_t target = s_target;
+        if (!bounded_spin([&] { return ld_acquire_u64(mine) >= target; }, timeout_ns, nullptr, 0u))
+            report_timeout(status, nullptr, 0u, kSiteBarrier, r, id);
+    }
+}
+
+sym_status_t sym_barrier(sym_win_t w, uint32_t signal_id, uint64_t timeout_ns, sym_stream_t stream) {
+    if (!w || signal_id >= w->nsignals) return SYM_ERR_INVALID_ARG;
+    if (timeout_ns == 0) timeout_ns = default_timeout_ns();
+    if (timeout_ns > 60000000000ull) timeout_ns = 60000000000ull;
+    DeviceGuard g(w->device);
+    if (!g.ok) return SYM_ERR_CUDA;
+    uint64_t* sig = w->sig;
+    uint32_t nsig = w->nsignals, id = signal_id;
+    int R = w->R;
+    uint32_t* status = w->ctx->status;
+    void* args[] = {&sig, &nsig, &id, &R, &timeout_ns, &status};
+    // ranks wait on one another -> co-resident blocks
+    SYM_CUDA(cudaLaunchCooperativeKernel((const void*)k_barrier, dim3((unsigned)R), dim3(kMaxRanks),
+                                         args, 0, (cudaStream_t)stream));
+    count_launch();
+    SYM_CUDA(cudaGetLastError());
+    return SYM_OK;
+}
+
 sym_status_t sym_signal(sym_win_t dst, int peer, uint32_t signal_id, uint64_t value,
                         sym_stream_t stream) {
     if (!dst || peer < 0 || peer >= dst->R || signal_id >= dst->nsignals) return SYM_ERR_INVALID_ARG;

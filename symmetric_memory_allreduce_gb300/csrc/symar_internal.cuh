@@ -32,6 +32,7 @@ enum WaitSite : uint32_t {
     kSitePutSignalRecv = 4,
     kSiteBulkStage = 5,
     kSiteSignalChain = 6,      // a put waited for the previous batch's signal of its pair
+    kSiteBarrier = 7,          // a rank waited at a barrier for the other ranks' signals
 };
 
 // Per-device context: the status block and the arrival ring used by

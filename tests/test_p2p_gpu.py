@@ -320,3 +320,32 @@ def test_get_reads_peer_into_local(symar, oracle):
     finally:
         remote.free()
         local.free()
+
+
+@pytest.mark.parametrize("R", [1, 3, 8, 64])
+def test_barrier_adds_R_per_call(symar, R):
+    """[GIN] barrier session, signal form: each call adds exactly R to every
+    rank's slot and returns once all R adds have arrived, also when recorded in
+    a CUDA graph and replayed."""
+    import torch
+
+    w = symar.Window(R, 4096, nsignals=2)
+    try:
+        for k in range(1, 4):
+            symar.sym_barrier(w, 1, timeout_ns=1_000_000_000)
+            assert symar.sym_stream_status() == symar.SYM_OK
+            for r in range(R):
+                assert symar.sym_signal_read(w, r, 1) == k * R
+                assert symar.sym_signal_read(w, r, 0) == 0
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            symar.sym_barrier(w, 1, timeout_ns=1_000_000_000, stream=s)
+        for k in range(4, 7):
+            g.replay()
+            torch.cuda.synchronize()
+            assert symar.sym_stream_status() == symar.SYM_OK
+            assert all(symar.sym_signal_read(w, r, 1) == k * R for r in range(R))
+    finally:
+        w.free()
