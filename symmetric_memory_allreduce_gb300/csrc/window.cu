@@ -517,8 +517,12 @@ sym_status_t sym_stream_status(sym_stream_t stream) {
     uint32_t st[4] = {0, 0, 0, 0};
     SYM_CUDA(cudaMemcpy(st, c->status, sizeof st, cudaMemcpyDeviceToHost));
     if (st[0] == 0) return SYM_OK;
-    snprintf(g_last_error, sizeof g_last_error, "device status 0x%x at site %u (%u, %u)", st[0],
-             st[1], st[2], st[3]);
+    static const char* const kSiteNames[] = {"none", "signal wait", "counter wait", "pull tile flag",
+                                             "put+signal/AlltoAll receiver", "bulk-copy stage",
+                                             "put+signal batch order", "barrier"};
+    const char* name = st[1] < sizeof kSiteNames / sizeof kSiteNames[0] ? kSiteNames[st[1]] : "?";
+    snprintf(g_last_error, sizeof g_last_error, "device status 0x%x at site %u (%s) (%u, %u)", st[0],
+             st[1], name, st[2], st[3]);
     SYM_CUDA(cudaMemset(c->status, 0, sizeof st));
     if (st[0] & kStatusTimeout) return SYM_ERR_TIMEOUT;
     return SYM_ERR_DEVICE_STATUS;
