@@ -15,6 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsymar.so")
+TOOL = os.path.join(HERE, "symar_bench")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -37,7 +38,8 @@ def _newest_input() -> float:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
+    if (not force and os.path.exists(LIB) and os.path.exists(TOOL)
+            and min(os.path.getmtime(LIB), os.path.getmtime(TOOL)) >= _newest_input()):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
@@ -62,6 +64,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    # the native benchmark of the C ABI (csrc/symar_bench.cu), linked against the library
+    tool_tmp = TOOL + f".tmp{os.getpid()}"
+    cmd = [cc, *ARCH, *NVCC_FLAGS, os.path.join(CSRC, "symar_bench.cu"), "-o", tool_tmp, "-L", HERE,
+           "-lsymar", "-Xlinker", "-rpath,$ORIGIN"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"symar_bench build failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tool_tmp, TOOL)
     return LIB
 
 
