@@ -819,7 +819,7 @@ sym_status_t sym_get(sym_win_t remote, sym_win_t local, int rank, int peer, size
     a.sig = nullptr;
     a.cnt = counter_id != UINT32_MAX ? local->cnt + (size_t)rank * local->ncounters + counter_id
                                      : nullptr;
-    a.arrive = ctx->arrive + (ctx->arrive_next++ % kArriveRing);
+    a.arrive = ctx->arrive + (ctx->arrive_next.fetch_add(1, std::memory_order_relaxed) % kArriveRing);
     const size_t per_cta = 64 * 1024;
     const size_t grid = std::max((size_t)1, std::min(ceil_div(bytes, per_cta),
                                                      (size_t)ctx->num_sms * 4));
@@ -852,7 +852,7 @@ sym_status_t sym_put_signal(sym_win_t src, sym_win_t dst, int src_rank, int peer
     a.sig = signal_id != UINT32_MAX ? dst->sig + (size_t)peer * dst->nsignals + signal_id : nullptr;
     a.cnt = counter_id != UINT32_MAX ? src->cnt + (size_t)src_rank * src->ncounters + counter_id
                                      : nullptr;
-    a.arrive = ctx->arrive + (ctx->arrive_next++ % kArriveRing);
+    a.arrive = ctx->arrive + (ctx->arrive_next.fetch_add(1, std::memory_order_relaxed) % kArriveRing);
     const size_t per_cta = 64 * 1024;
     const size_t grid = std::max((size_t)1, std::min(ceil_div(bytes, per_cta),
                                                      (size_t)ctx->num_sms * 4));

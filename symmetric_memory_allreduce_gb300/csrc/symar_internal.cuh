@@ -36,7 +36,9 @@ enum WaitSite : uint32_t {
 };
 
 // Per-device context: the status block and the arrival ring used by
-// multi-CTA puts to find the last CTA.
+// multi-CTA puts (and gets) to find the last CTA.  Each launch takes the next
+// of kArriveRing counters, so up to that many such launches may be in flight
+// at once on a device, across all streams.
 //
 // status[0] bits, [1] site, [2..3] coordinates of the first wait that ran out
 // (read and cleared by sym_stream_status).  A launch's other waits stop early
@@ -46,7 +48,7 @@ struct DevCtx {
     int num_sms = 0;
     uint32_t* status = nullptr;   // kStatusWords words, see above
     uint32_t* arrive = nullptr;   // kArriveRing counters, zero when idle
-    uint64_t arrive_next = 0;     // host-side ring cursor
+    std::atomic<uint64_t> arrive_next{0};   // host-side ring cursor (calls from several threads)
 };
 constexpr int kArriveRing = 1024;
 constexpr int kStatusWords = 8;
