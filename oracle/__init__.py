@@ -9,9 +9,10 @@ built with ``-O2 -ffp-contract=off -fno-fast-math``); this module only builds
 it with gcc, loads it with ctypes and marshals numpy arrays.
 
 Parity status: every function is pinned by ``tests/test_oracle.py`` to facts
-that do not come from this code, except ``rolling_le``, which is "parity
-unpinned" (the GIN reference page cites a rolling comparison without printing
-it; the reading taken is documented in ``oracle.c``).
+that do not come from this code.  ``rolling_le`` (the GIN reference page names a
+rolling comparison without printing it) is pinned to RFC 1982 serial number
+arithmetic and to the page's x <= x+1 property; the reading taken where the RFC
+is undefined is documented in ``oracle.c``.
 """
 from __future__ import annotations
 
@@ -214,7 +215,7 @@ def prefix_mismatch(src_q: np.ndarray, seg: np.ndarray, chunk: int, batch: int, 
 
 
 def rolling_le(a: int, b: int, bits: int = 64) -> bool:
-    """PARITY UNPINNED reading of the rolling comparison (see oracle.c)."""
+    """Rolling a <= b on the low `bits` bits (reading and pins in oracle.c)."""
     return bool(_load().oracle_rolling_le(a & (2**64 - 1), b & (2**64 - 1), bits))
 
 

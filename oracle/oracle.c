@@ -21,9 +21,11 @@
  *           of a batch of puts followed by one signal; section 5.3: batches of
  *           at most 8 commands with one signalled request per batch).
  *
- * Parity status of each function is stated in its comment.  One function,
- * oracle_rolling_le, is "parity unpinned": the page refers to a rolling
- * comparison pseudo-code without printing it (see its comment).
+ * Parity status of each function is stated in its comment.  Every function is
+ * pinned by tests/test_oracle.py to facts that do not come from this file.
+ * oracle_rolling_le, whose formula the page names without printing, is pinned
+ * to RFC 1982 serial number arithmetic (the published definition of such a
+ * comparison) and to the page's stated property (see its comment).
  */
 #include <stddef.h>
 #include <stdint.h>
@@ -409,12 +411,18 @@ uint64_t oracle_prefix_mismatch(size_t S, size_t chunk, size_t B, uint64_t k,
 }
 
 /* ------------------------------------------------------------------------ */
-/* Rolling comparison.  PARITY UNPINNED (formula not printed on the page).  */
+/* Rolling comparison.                                                      */
 /* [GIN] "Signals and Counters": signal and counter values are compared     */
 /* with a rolling rule so that x <= x+1 holds even across unsigned          */
 /* overflow; waitSignal(least, bits) returns once the low `bits` bits of    */
-/* the value are rolling-greater-or-equal to `least`.  Reading taken: with  */
-/* m = 2^bits - 1 and d = (b - a) mod 2^bits, a <= b iff d < 2^(bits-1).    */
+/* the value are rolling-greater-or-equal to `least`.  The page names the   */
+/* routine without printing it.  Reading taken: with m = 2^bits - 1 and     */
+/* d = (b - a) mod 2^bits, a <= b iff d < 2^(bits-1), i.e. b is one of the  */
+/* 2^(bits-1) values a, a+1, ... (mod 2^bits).                              */
+/* Pins: RFC 1982 (Serial Number Arithmetic) "less than" in its case form,  */
+/* exhaustively for 1..10 bits, with the pair exactly 2^(bits-1) apart      */
+/* (undefined there) read as "not reached"; the page's x <= x+1 for every   */
+/* x; integer <= where nothing wraps; 56/63/64-bit edges with high bits.    */
 /* ------------------------------------------------------------------------ */
 int oracle_rolling_le(uint64_t a, uint64_t b, int bits)
 {

@@ -291,27 +291,141 @@ def test_prefix_mismatch(oracle):
     assert oracle.prefix_mismatch(src, seg, chunk, B, 99) == 1
 
 
-# ---------------------------------------------------------------- rolling compare (unpinned)
+# ---------------------------------------------------------------- rolling compare
+#
+# [GIN] "Signals and Counters": signal and counter values are compared with a
+# rolling rule under which x <= x+1 holds even across unsigned overflow, and
+# waitSignal / waitCounter return once the low `bits` bits of the value have
+# reached or passed `least`.  The page names the routine but does not print
+# it.  The pins below come from outside the oracle:
+#  * RFC 1982 ("Serial Number Arithmetic"), the published definition of such a
+#    comparison, written here in its own case form: i1 < i2 when
+#    (i1 < i2 and i2 - i1 < 2^(n-1)) or (i1 > i2 and i1 - i2 > 2^(n-1)); the
+#    RFC leaves the pair exactly 2^(n-1) apart undefined, and the reading taken
+#    there is "not reached yet" (the wait goes on);
+#  * the half-open window: `b` is rolling->= `a` iff b is one of the 2^(n-1)
+#    values a, a+1, ..., a+2^(n-1)-1 (mod 2^n), enumerated as a set;
+#  * the page's property (x <= x, x <= x+1 for every x, wrap included), and
+#    plain integer <= wherever no wrap is involved ("reached or passed").
 
-def test_rolling_le_truth_table(oracle):
-    """Only the page's stated property is pinned: x <= x and x <= x+1 across wrap."""
-    M = 2**64 - 1
-    assert oracle.rolling_le(0, 0)
-    assert not oracle.rolling_le(5, 4)
-    assert oracle.rolling_le(4, 5)
-    assert oracle.rolling_le(M, 0)                  # x <= x+1 across overflow
-    assert not oracle.rolling_le(0, M)
-    assert not oracle.rolling_le(0, 2**63)          # reading: half-range is "behind"
-    assert oracle.rolling_le(0, 2**63 - 1)
+
+def _rfc1982_lt(i1: int, i2: int, n: int) -> bool | None:
+    """RFC 1982 section 3.2 'less than' on n-bit serial numbers; None where undefined."""
+    half = 1 << (n - 1)
+    if i1 == i2:
+        return False
+    if abs(i1 - i2) == half:
+        return None
+    return (i1 < i2 and i2 - i1 < half) or (i1 > i2 and i1 - i2 > half)
+
+
+def _window_le(a: int, b: int, n: int) -> bool:
+    """b in the set {a + k mod 2^n : 0 <= k < 2^(n-1)}."""
+    mod = 1 << n
+    return b % mod in {(a + k) % mod for k in range(1 << (n - 1))}
+
+
+def test_rolling_le_exhaustive_small_widths(oracle):
+    """Every (a, b) for widths 1..10 bits against the RFC 1982 case form and the window set."""
+    for n in range(1, 11):
+        mod = 1 << n
+        windows = [{(a + k) % mod for k in range(1 << (n - 1))} for a in range(mod)]
+        for a in range(mod):
+            for b in range(mod):
+                got = oracle.rolling_le(a, b, n)
+                assert got == (b in windows[a]), (n, a, b)
+                lt = _rfc1982_lt(a, b, n)
+                if lt is not None:
+                    assert got == (a == b or lt), (n, a, b)
+                else:
+                    assert not got, (n, a, b)      # the pair 2^(n-1) apart: not reached
+
+
+def test_rolling_le_page_properties(oracle):
+    """x <= x and x <= x+1 for every x (wrap included); x+1 <= x never.  From 2 bits up:
+    with 1 bit, x+1+1 == x, so no order can have both; there only x <= x holds."""
+    for x in (0, 1):
+        assert oracle.rolling_le(x, x, 1) and not oracle.rolling_le(x, x ^ 1, 1)
+    for n in list(range(2, 13)) + [31, 32, 33, 55, 56, 57, 63, 64]:
+        mod = 1 << n
+        xs = range(mod) if n <= 12 else [0, 1, 2, mod // 2 - 1, mod // 2, mod // 2 + 1, mod - 2,
+                                         mod - 1]
+        for x in xs:
+            assert oracle.rolling_le(x, x, n)
+            assert oracle.rolling_le(x, (x + 1) % mod, n), (n, x)
+            assert not oracle.rolling_le((x + 1) % mod, x, n), (n, x)
+
+
+def test_rolling_le_agrees_with_integer_order_without_wrap(oracle):
+    """While both values stay below 2^(n-1) nothing wraps: rolling <= is integer <=."""
+    rng = np.random.default_rng(1982)
+    for n in range(2, 11):
+        half = 1 << (n - 1)
+        for a in range(half):
+            for b in range(half):
+                assert oracle.rolling_le(a, b, n) == (a <= b), (n, a, b)
+    for n in (16, 32, 55, 56, 57, 63, 64):
+        half = 1 << (n - 1)
+        for _ in range(2000):
+            a, b = (int(v) for v in rng.integers(0, half, 2, dtype=np.uint64))
+            assert oracle.rolling_le(a, b, n) == (a <= b), (n, a, b)
+
+
+def test_rolling_le_wide_edges(oracle):
+    """Widths 56 (counters), 63 and 64 (signals) at the wrap and at the half-range edge,
+    with values above the mask (only the low n bits count)."""
+    rng = np.random.default_rng(56)
+    for n in (56, 63, 64):
+        mod, half = 1 << n, 1 << (n - 1)
+        for a in [0, 1, half - 1, half, half + 1, mod - 1] + [int(v) for v in
+                                                              rng.integers(0, mod, 20, dtype=np.uint64)]:
+            for d in [0, 1, 2, half - 2, half - 1, half, half + 1, mod - 2, mod - 1]:
+                b = (a + d) % mod
+                want = d < half
+                assert oracle.rolling_le(a, b, n) == want, (n, a, d)
+                lt = _rfc1982_lt(a, b, n)
+                if lt is not None:
+                    assert want == (a == b or lt)
+                if n < 64:                         # bits above the mask are ignored, both sides
+                    hi = int(rng.integers(1, 1 << (64 - n))) << n
+                    assert oracle.rolling_le(a, b | hi, n) == want
+                    assert oracle.rolling_le(a | hi, b, n) == want
     m56 = 2**56 - 1
-    assert oracle.rolling_le(m56, 0, 56)            # 56-bit counters wrap at 2^56
-    assert oracle.rolling_le(m56, 2**56, 56)        # high bits ignored
+    assert oracle.rolling_le(m56, 0, 56)             # 56-bit counters wrap at 2^56
+    assert oracle.rolling_le(m56, 2**56, 56)
     assert not oracle.rolling_le(1, 0, 56)
-    for x in [0, 1, 2**32, 2**63, M]:
-        assert oracle.rolling_le(x, x + 1)
-        assert oracle.rolling_le(x, x)
     assert oracle.read_bits(2**60 + 5, 56) == 5
-    assert oracle.read_bits(M, 64) == M
+    assert oracle.read_bits(2**64 - 1, 64) == 2**64 - 1
+
+
+def test_rolling_pins_catch_plausible_mistakes():
+    """Each pin rejects a plausible wrong formula (checked here on Python stand-ins)."""
+    def ok(a, b, n):
+        m = (1 << n) - 1
+        return ((b - a) & m) < (1 << (n - 1))
+
+    wrong = {
+        "<= half": lambda a, b, n: ((b - a) & ((1 << n) - 1)) <= (1 << (n - 1)),
+        "operands swapped": lambda a, b, n: ((a - b) & ((1 << n) - 1)) < (1 << (n - 1)),
+        "full range": lambda a, b, n: ((b - a) & ((1 << n) - 1)) < (1 << n),
+        "plain integer": lambda a, b, n: a <= b,
+        "no mask": lambda a, b, n: ((b - a) % (1 << 64)) < (1 << (n - 1)),
+    }
+
+    def passes(f):
+        for n in range(1, 7):
+            mod = 1 << n
+            for a in range(mod):
+                for b in range(mod):
+                    if f(a, b, n) != _window_le(a, b, n):
+                        return False
+                if n >= 2 and not f(a, (a + 1) % mod, n):
+                    return False
+        return True
+
+    assert passes(ok)
+    for name, f in wrong.items():
+        assert not passes(f), name
 
 
 # ---------------------------------------------------------------- fp16 rounding

@@ -226,6 +226,66 @@ def test_rolling_wait_semantics(symar, oracle):
         w.free()
 
 
+def _rolling_cases(rng):
+    """(least, value, bits) around the wrap and the half-range edge, with high bits set."""
+    cases = []
+    for n in (1, 2, 3, 7, 8, 16, 32, 55, 56, 57, 63, 64):
+        mod, half = 1 << n, 1 << (n - 1)
+        anchors = sorted({0, 1, half - 1, half, mod - 1, int(rng.integers(0, mod, dtype=np.uint64))})
+        for a in anchors:
+            for d in sorted({0, 1, half - 1, half, half + 1, mod - 1} - {mod}):
+                v = (a + d) % mod
+                least = a
+                if n < 64:                      # bits above the mask must not matter
+                    v |= int(rng.integers(0, 1 << (64 - n), dtype=np.uint64)) << n
+                    least |= int(rng.integers(0, 1 << (64 - n), dtype=np.uint64)) << n
+                cases.append((least, v, n))
+    return cases
+
+
+def test_rolling_wait_sweep_matches_oracle(symar, oracle):
+    """sym_signal_wait ends (SYM_OK) or runs out (SYM_ERR_TIMEOUT, 1 ms bound) exactly when the
+    oracle's rolling_le(least, value, bits) says the value has or has not reached `least`:
+    [GIN] "Signals and Counters", waitSignal(least, bits) on the rolling comparison."""
+    cases = _rolling_cases(np.random.default_rng(1982))
+    w = symar.Window(1, 4096, nsignals=len(cases))
+    try:
+        for i, (_, v, _) in enumerate(cases):
+            if v:
+                symar.sym_signal(w, 0, i, v)             # slots start at 0
+        assert symar.sym_stream_status() == symar.SYM_OK
+        reached = timed_out = 0
+        for i, (least, v, n) in enumerate(cases):
+            assert symar.sym_signal_read(w, 0, i) == v
+            want = oracle.rolling_le(least, v, n)
+            symar.sym_signal_wait(w, 0, i, least, bits=n, timeout_ns=1_000_000)
+            st = symar.sym_stream_status()
+            assert st == (symar.SYM_OK if want else symar.SYM_ERR_TIMEOUT), (hex(least), hex(v), n)
+            reached += want
+            timed_out += not want
+        assert reached > 100 and timed_out > 100
+    finally:
+        w.free()
+
+
+def test_rolling_counter_wait_matches_oracle(symar, oracle):
+    """waitCounter on 1..3 low bits of a counter at 3 (three puts): the rolling outcome, not <=."""
+    src, dst = symar.Window(2, 4096, ncounters=1), symar.Window(2, 4096, nsignals=1)
+    try:
+        for _ in range(3):
+            symar.sym_put_signal(src, dst, 0, 1, 0, 16, 32, counter_id=0)
+        assert symar.sym_counter_read(src, 0, 0) == 3
+        for n in (1, 2, 3, 56):
+            for least in range(8):
+                want = oracle.rolling_le(least, 3, n)
+                symar.sym_counter_wait(src, 0, 0, least, bits=n, timeout_ns=1_000_000)
+                st = symar.sym_stream_status()
+                assert st == (symar.SYM_OK if want else symar.SYM_ERR_TIMEOUT), (least, n)
+    finally:
+        src.free()
+        dst.free()
+
+
 def test_counter_56_bits(symar):
     src, dst = symar.Window(2, 4096, ncounters=1), symar.Window(2, 4096, nsignals=1)
     try:
