@@ -54,7 +54,9 @@
 extern "C" {
 #endif
 
-#define SYMAR_ABI_VERSION 1
+/* 2: sym_algo_t takes the values of the library's first published table
+ * (SYM_ALGO_PUT_SIGNAL = 3; algorithms added later follow it). */
+#define SYMAR_ABI_VERSION 2
 
 typedef struct sym_window* sym_win_t;   /* opaque handle */
 typedef void* sym_stream_t;             /* a cudaStream_t */
@@ -74,15 +76,18 @@ typedef enum { SYM_SUM = 0, SYM_MAX = 1, SYM_MIN = 2 } sym_op_t;
 
 typedef enum {
     SYM_ALGO_AUTO = 0,
-    /* AllReduce */
-    SYM_ALGO_ONESHOT = 1,        /* every rank-slot reads all R windows, writes its own */
-    SYM_ALGO_TWOSHOT = 2,        /* reduce-scatter by loads + all-gather by stores, 1 launch */
-    SYM_ALGO_TWOSHOT_PULL = 3,   /* reduce-scatter, per-tile release flags, pull all-gather, 1 launch */
-    SYM_ALGO_TWOSHOT_SPLIT = 4,  /* reduce-scatter launch, then pull all-gather launch */
-    /* AllGather */
-    SYM_ALGO_COPY = 5,           /* read each segment once, store it to all R ranks */
-    SYM_ALGO_PUT_SIGNAL = 6,     /* chunked puts, one strong signal per batch, receivers wait */
-    SYM_ALGO_CE = 7              /* copy engines, no kernel: one 1-D memcpy per (sender, destination) */
+    SYM_ALGO_ONESHOT = 1,        /* AllReduce: every rank-slot reads all R windows, writes its own */
+    SYM_ALGO_TWOSHOT = 2,        /* AllReduce: reduce-scatter by loads + all-gather by stores, 1 launch */
+    SYM_ALGO_PUT_SIGNAL = 3,     /* AllGather / AlltoAll: chunked puts, one strong signal per batch,
+                                    receivers wait */
+    /* values added after the four above; existing values never change */
+    SYM_ALGO_TWOSHOT_PULL = 4,   /* AllReduce: reduce-scatter, per-tile release flags, pull all-gather,
+                                    1 launch */
+    SYM_ALGO_TWOSHOT_SPLIT = 5,  /* AllReduce: reduce-scatter launch, then pull all-gather launch */
+    SYM_ALGO_COPY = 6,           /* AllGather / AlltoAll: read each segment once, store it to all R
+                                    ranks */
+    SYM_ALGO_CE = 7              /* AllGather: copy engines, no kernel: one 1-D memcpy per (sender,
+                                    destination) */
 } sym_algo_t;
 
 /* ---------------------------------------------------------------- windows */
@@ -165,7 +170,9 @@ sym_status_t sym_window_read(sym_win_t w, int rank, size_t off, void* dst, size_
  * stream) on symmetric windows; each element is the sum over all ranks.
  * count: elements per rank; count*sizeof(dtype) <= bytes of both windows.
  * send == recv (in place) is allowed for the two-shot algorithms, not for
- * ONESHOT.  count == 0 is a no-op.  AUTO picks ONESHOT up to
+ * ONESHOT.  Two different windows must not share a byte of the ranges the
+ * call touches (possible with sym_window_register): INVALID_ARG, checked on
+ * the host.  count == 0 is a no-op.  AUTO picks ONESHOT up to
  * SYM_ONESHOT_MAX_BYTES per rank (env, default 128 KiB), else TWOSHOT.
  * TWOSHOT_PULL enqueues a one-thread kernel that advances the recv window's
  * flag epoch on the device before the main launch, so the call can be
@@ -211,7 +218,8 @@ sym_status_t sym_allreduce_algo(sym_win_t send, size_t count, sym_dtype_t dtype,
 /* AllGather: recv_r[q*S + i] = send_q[i] for all ranks r, q and bytes
  * i < S = sendcount*sizeof(dtype).  [SYMEX] Example 2: the receive buffer
  * holds sendcount*nranks elements and segment q holds rank q's data.
- * recv bytes_per_rank >= R*S.  send and recv must be different windows.
+ * recv bytes_per_rank >= R*S.  send and recv must be different windows that
+ * share no byte of the ranges the call touches (INVALID_ARG).
  * algo: AUTO or COPY (SM kernel: each 16 KiB segment tile is loaded once
  * into shared memory by a bulk copy and stored to the R ranks by R bulk
  * copies; env SYM_ALLGATHER_KERNEL=ldst selects a register load/store kernel
@@ -271,7 +279,8 @@ sym_status_t sym_allgather_put_signal(sym_win_t send, sym_win_t recv, size_t byt
  * algo PUT_SIGNAL: the same copies, each followed by a release increment of
  * signal slot 0 of the receiving rank (reset to 0 first, stream-ordered), and
  * receivers in the same launch wait (bounded by timeout_ns, 0 = default)
- * until it reaches R; requires recv nsignals >= 1.  send != recv.
+ * until it reaches R; requires recv nsignals >= 1.  send and recv must be
+ * different windows that share no byte of the ranges the call touches.
  * Errors: INVALID_ARG, CUDA; a wait that runs out -> SYM_ERR_TIMEOUT from
  * sym_stream_status(). */
 sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtype_t dtype,
@@ -285,7 +294,8 @@ sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtyp
  * publishes the tile's flag with a release store, and the reduction of that
  * tile starts as soon as it acquires the flag, overlapping the production of
  * later tiles.  alpha: host array of R floats (copied at the call).  f32
- * only; the three windows must have the same R and be distinct.  count
+ * only; the three windows must have the same R and share no byte of the
+ * ranges the call touches.  count
  * elements per rank.  Errors: INVALID_ARG, UNSUPPORTED, CUDA; a wait that
  * runs out -> SYM_ERR_TIMEOUT from sym_stream_status(). */
 sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_win_t recv, const float* alpha,
@@ -347,8 +357,11 @@ sym_status_t sym_signal(sym_win_t dst, int peer, uint32_t signal_id, uint64_t va
 sym_status_t sym_signal_wait(sym_win_t w, int rank, uint32_t signal_id, uint64_t least, int bits,
                              uint64_t timeout_ns, sym_stream_t stream);
 
-/* Read the low `bits` bits of a signal after the work queued on `stream`
- * ([GIN] readSignal); synchronises `stream`. */
+/* Read the low `bits` bits (1..64) of a signal after the work queued on
+ * `stream` ([GIN] readSignal(signal, bits)); synchronises `stream`.  `bits`
+ * and `stream` extend the first published signature (w, rank, id, out):
+ * readSignal takes a width, and on one GPU the read must be ordered after the
+ * stream's own puts. */
 sym_status_t sym_signal_read(sym_win_t w, int rank, uint32_t signal_id, int bits, uint64_t* out,
                              sym_stream_t stream);
 
@@ -356,7 +369,9 @@ sym_status_t sym_signal_read(sym_win_t w, int rank, uint32_t signal_id, int bits
 sym_status_t sym_signal_reset(sym_win_t w, int rank, uint32_t signal_id, sym_stream_t stream);
 
 /* Counters ([GIN] readCounter / waitCounter / resetCounter): the same as the
- * signal calls, on counter slots; values are read through at most 56 bits. */
+ * signal calls, on counter slots; values are read through at most 56 bits
+ * (bits 1..56).  sym_counter_read takes `bits` and `stream` for the same
+ * reasons as sym_signal_read. */
 sym_status_t sym_counter_read(sym_win_t w, int rank, uint32_t counter_id, int bits, uint64_t* out,
                               sym_stream_t stream);
 sym_status_t sym_counter_wait(sym_win_t w, int rank, uint32_t counter_id, uint64_t least, int bits,

@@ -22,9 +22,9 @@ SYM_OK, SYM_ERR_INVALID_ARG, SYM_ERR_OOM, SYM_ERR_CUDA = 0, 1, 2, 3
 SYM_ERR_TIMEOUT, SYM_ERR_UNSUPPORTED, SYM_ERR_DEVICE_STATUS = 4, 5, 6
 SYM_F32, SYM_BF16, SYM_F16 = 0, 1, 2
 SYM_SUM, SYM_MAX, SYM_MIN = 0, 1, 2
-SYM_ALGO_AUTO, SYM_ALGO_ONESHOT, SYM_ALGO_TWOSHOT = 0, 1, 2
-SYM_ALGO_TWOSHOT_PULL, SYM_ALGO_TWOSHOT_SPLIT = 3, 4
-SYM_ALGO_COPY, SYM_ALGO_PUT_SIGNAL, SYM_ALGO_CE = 5, 6, 7
+SYM_ALGO_AUTO, SYM_ALGO_ONESHOT, SYM_ALGO_TWOSHOT, SYM_ALGO_PUT_SIGNAL = 0, 1, 2, 3
+SYM_ALGO_TWOSHOT_PULL, SYM_ALGO_TWOSHOT_SPLIT = 4, 5
+SYM_ALGO_COPY, SYM_ALGO_CE = 6, 7
 SYM_WINDOW_CUDA_MALLOC, SYM_WINDOW_REGISTERED, SYM_WINDOW_VMM_EXPORTABLE, SYM_WINDOW_VMM = 0, 1, 2, 3
 NO_ID = 0xFFFFFFFF
 

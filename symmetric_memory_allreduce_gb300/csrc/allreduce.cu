@@ -32,7 +32,9 @@ sym_status_t sym_allreduce(sym_win_t send, sym_win_t recv, size_t count, sym_dty
     const size_t es = dtype_size(dtype);
     if (!es) return SYM_ERR_INVALID_ARG;
     if ((int)op < SYM_SUM || (int)op > SYM_MIN) return SYM_ERR_INVALID_ARG;
-    if ((int)algo < SYM_ALGO_AUTO || (int)algo > SYM_ALGO_TWOSHOT_SPLIT) return SYM_ERR_INVALID_ARG;
+    if (algo != SYM_ALGO_AUTO && algo != SYM_ALGO_ONESHOT && algo != SYM_ALGO_TWOSHOT &&
+        algo != SYM_ALGO_TWOSHOT_PULL && algo != SYM_ALGO_TWOSHOT_SPLIT)
+        return SYM_ERR_INVALID_ARG;
     if (count > send->bytes / es || count > recv->bytes / es) return SYM_ERR_INVALID_ARG;
     if (count == 0) return SYM_OK;
     const bool in_place = send->base == recv->base;
@@ -41,6 +43,12 @@ sym_status_t sym_allreduce(sym_win_t send, sym_win_t recv, size_t count, sym_dty
     algo = resolve_algo(algo, nbytes, in_place);
     if (in_place && algo == SYM_ALGO_ONESHOT) return SYM_ERR_UNSUPPORTED;
     if (in_place && send != recv) return SYM_ERR_INVALID_ARG;   // two handles, one memory
+    if (!in_place && windows_overlap(send, nbytes, recv, nbytes)) {
+        // partly aliased windows (caller memory): one-shot would race, and the
+        // pull gathers would read inputs another slot has overwritten
+        set_last_error("sym_allreduce: send and recv windows share memory without being one window");
+        return SYM_ERR_INVALID_ARG;
+    }
 
     ArArgs a{};
     a.send = send->base;

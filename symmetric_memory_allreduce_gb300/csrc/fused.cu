@@ -157,6 +157,11 @@ extern "C" sym_status_t sym_scale_allreduce(sym_win_t in, sym_win_t send, sym_wi
         return SYM_ERR_INVALID_ARG;
     if (count == 0) return SYM_OK;
     const size_t nbytes = count * 4;
+    if (windows_overlap(in, nbytes, send, nbytes) || windows_overlap(send, nbytes, recv, nbytes) ||
+        windows_overlap(in, nbytes, recv, nbytes)) {
+        set_last_error("sym_scale_allreduce: two of the three windows share memory");
+        return SYM_ERR_INVALID_ARG;
+    }
     if (nbytes / kVecBytes > ((size_t)1 << 34)) return SYM_ERR_UNSUPPORTED;
     FusedArgs a{};
     a.in = in->base;

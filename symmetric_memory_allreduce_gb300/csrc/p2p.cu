@@ -659,6 +659,10 @@ sym_status_t sym_allgather(sym_win_t send, sym_win_t recv, size_t sendcount, sym
     const size_t S = sendcount * es;
     if (S > recv->bytes / (size_t)R) return SYM_ERR_INVALID_ARG;
     if (S == 0) return SYM_OK;
+    if (windows_overlap(send, S, recv, (size_t)R * S)) {
+        set_last_error("sym_allgather: send and recv windows share memory");
+        return SYM_ERR_INVALID_ARG;
+    }
     DeviceGuard g(recv->device);
     if (!g.ok) return SYM_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
@@ -722,6 +726,10 @@ sym_status_t sym_allgather_put_signal(sym_win_t send, sym_win_t recv, size_t byt
     if (bytes_per_rank > send->bytes || bytes_per_rank > recv->bytes / (size_t)R)
         return SYM_ERR_INVALID_ARG;
     if (bytes_per_rank == 0) return SYM_OK;
+    if (windows_overlap(send, bytes_per_rank, recv, (size_t)R * bytes_per_rank)) {
+        set_last_error("sym_allgather_put_signal: send and recv windows share memory");
+        return SYM_ERR_INVALID_ARG;
+    }
     DeviceGuard g(recv->device);
     if (!g.ok) return SYM_ERR_CUDA;
     sym_status_t s = launch_put_signal_allgather(send, recv, bytes_per_rank, chunk_bytes,
@@ -746,6 +754,10 @@ sym_status_t sym_alltoall(sym_win_t send, sym_win_t recv, size_t count, sym_dtyp
     const bool signalled = algo == SYM_ALGO_PUT_SIGNAL;
     if (signalled && recv->nsignals < 1) return SYM_ERR_INVALID_ARG;
     if (count == 0) return SYM_OK;
+    if (windows_overlap(send, (size_t)R * count * es, recv, (size_t)R * count * es)) {
+        set_last_error("sym_alltoall: send and recv windows share memory");
+        return SYM_ERR_INVALID_ARG;
+    }
     DeviceGuard g(recv->device);
     if (!g.ok) return SYM_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;

@@ -94,6 +94,11 @@ void set_last_error(const char* text);                      // text for sym_last
         if (e_ != cudaSuccess) return ::symar::cuda_fail(e_, #call);     \
     } while (0)
 
+// True when a byte of some rank's range [0, a_bytes) of window `a` is also a
+// byte of some rank's range [0, b_bytes) of window `b` (caller memory can make
+// two windows alias; interleaved windows that share no byte are not flagged).
+bool windows_overlap(const sym_window* a, size_t a_bytes, const sym_window* b, size_t b_bytes);
+
 // Makes `w->device` current for the scope, restoring the previous device.
 struct DeviceGuard {
     int prev = -1;

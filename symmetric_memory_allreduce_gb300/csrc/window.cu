@@ -36,6 +36,24 @@ void set_last_error(const char* text) {
     snprintf(g_last_error, sizeof g_last_error, "%s", text);
 }
 
+bool windows_overlap(const sym_window* a, size_t a_bytes, const sym_window* b, size_t b_bytes) {
+    if (a_bytes == 0 || b_bytes == 0) return false;
+    const uintptr_t a0 = (uintptr_t)a->base, b0 = (uintptr_t)b->base;
+    const uintptr_t a1 = a0 + (size_t)(a->R - 1) * a->stride + a_bytes;
+    const uintptr_t b1 = b0 + (size_t)(b->R - 1) * b->stride + b_bytes;
+    if (a1 <= b0 || b1 <= a0) return false;          // the extents are apart
+    // interleaved windows can share an extent without sharing a byte: compare
+    // the R x R rank ranges one by one (R <= 64)
+    for (int i = 0; i < a->R; ++i) {
+        const uintptr_t s = a0 + (size_t)i * a->stride, e = s + a_bytes;
+        for (int j = 0; j < b->R; ++j) {
+            const uintptr_t t = b0 + (size_t)j * b->stride;
+            if (s < t + b_bytes && t < e) return true;
+        }
+    }
+    return false;
+}
+
 DeviceGuard::DeviceGuard(int dev) {
     if (cudaGetDevice(&prev) != cudaSuccess) {
         prev = -1;
