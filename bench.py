@@ -229,8 +229,8 @@ def cpu_oracle_rate(x_sample, budget_s: float) -> dict:
         if el1 >= budget_s / 4:
             break
     return {"value": S * passes / el / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
-            "sample": f"R={R} x {n} fp32 elements per rank (first {S >> 20} MiB of each rank's "
-                      f"256 MiB input), {passes} passes in {el:.1f} s, {used} threads",
+            "sample": f"the whole workload: R={R} x {n} fp32 elements ({S >> 20} MiB) per rank, "
+                      f"{passes} passes in {el:.1f} s, {used} threads",
             "seconds_per_pass": el / passes, "single_thread_value": S * p1 / el1 / 1e9,
             "cpu_model": cpu_model()}
 
@@ -255,15 +255,14 @@ def cpu_model() -> str:
 
 
 def run_reference(args) -> int:
-    """The reference arm: the CPU oracle, rank 0 only."""
+    """The reference arm: the CPU oracle, rank 0 only, over the whole workload every step."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
-    R = R_DEFAULT
-    n_sample = 1 << 22            # 16 MiB per rank: one pass ~10-100 ms on a host
-    x = wl.uniform_f32(3, R, n_sample)
+    R, n = args.ranks, args.count
+    x = wl.uniform_f32(3, R, n) if n == N_DEFAULT else wl.normal_f32(4, R, n)
     import oracle
 
     oracle.build()
@@ -277,15 +276,17 @@ def run_reference(args) -> int:
         _, used = oracle.allreduce_sum_mt(x, nthreads)
         times.append(time.perf_counter() - t0)
     t = sum(times) / len(times)
-    S = n_sample * 4
+    S = n * 4
     value = S / t / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded U(-1,1) fp32, PCG64)",
-            "config": _config(R, N_DEFAULT, "oracle (CPU, rank order)"),
+            "vs_baseline": None, "dtype": "f32", "data": DATA,
+            "algo": "CPU oracle (rank-order fp32 sum per element, host threads)",
+            "config": _config(R, n),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": used, "kind": "oracle",
-                             "sample": f"R={R} x {n_sample} fp32 elements per rank per step",
+                             "sample": f"the whole workload every step: R={R} x {n} fp32 elements "
+                                       f"per rank, {used} threads",
                              "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -293,10 +294,14 @@ def run_reference(args) -> int:
     return 0
 
 
-def _config(R, n, algo):
+DATA = "synthetic (seeded U(-1,1) fp32 per rank, numpy PCG64)"
+
+
+def _config(R, n):
+    """The workload, identical in both arms (how it is computed is the line's `algo`)."""
     return {"workload": f"AllReduce(sum) R={R} rank windows x {n} fp32 elements "
                         f"({n * 4 >> 20} MiB) per rank, seeded U(-1,1)",
-            "R": R, "count_per_rank": n, "bytes_per_rank": n * 4, "algo": algo,
+            "R": R, "count_per_rank": n, "bytes_per_rank": n * 4,
             "l2": "inputs 2 GiB > 126 MiB L2 (no flush needed)", "parallelism": "replicas"}
 
 
@@ -388,17 +393,20 @@ def run_ours(args) -> int:
     if not args.no_e2e:
         e2e = run_e2e(sm, send, recv, x, R, n, args, world, stream)
 
+    secondary = None
+    if rank == 0 and world == 1 and not args.no_secondary and (R, n) == (R_DEFAULT, N_DEFAULT):
+        secondary = run_secondary(sm, stream, x, peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_rate(np.ascontiguousarray(x[:, : min(n, 1 << 24)]), args.cpu_seconds)
+        cpu = cpu_oracle_rate(x, args.cpu_seconds)
 
     traffic = recorded_traffic(R, S)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded U(-1,1) fp32 per rank, numpy PCG64)",
-        "config": _config(R, n, args.algo),
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": DATA,
+        "algo": args.algo, "config": _config(R, n),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "k_twoshot_st<F32T,8,1>" if args.algo in ("twoshot", "auto")
@@ -406,9 +414,13 @@ def run_ours(args) -> int:
                      "bytes_per_launch": bytes_model["compulsory"],
                      "kernel_ms": kern_ms, "kernel_ms_p10": percentile(per, 0.1),
                      "kernel_ms_p90": percentile(per, 0.9)},
-        "hbm_gbs": achieved, "hbm_pct_of_peak": 100.0 * achieved / peak,
+        # bytes actually read and written (ncu DRAM counters of this kernel) over its time
+        "hbm_gbs": traffic / (kern_ms * 1e-3) / 1e9 if traffic else None,
+        "hbm_pct_of_peak": 100.0 * traffic / (kern_ms * 1e-3) / 1e9 / peak if traffic else None,
+        "compulsory_gbs": achieved,
         "logical_gbs": bytes_model["logical"] / (kern_ms * 1e-3) / 1e9,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        "secondary": secondary,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -478,6 +490,143 @@ def run_e2e(sm, send, recv, x, R, n, args, world, stream) -> dict:
             "ms_per_step": e_ms,
             "host_link_gbs": 2 * R * S / (e_ms * 1e-3) / 1e9,
             "pipeline": "2 window pairs, 3 streams: copy-in || AllReduce || copy-out"}
+
+
+def run_secondary(sm, stream, x3, peak) -> list[dict]:
+    """The other measured rows, each timed over >= 20 launches (CUDA events per launch on the
+    library's stream, after 5 warm-ups) and checked against the oracle in the same run:
+    config 3 bf16 (two-shot, pull) and fp32 pull, config 2 one-shot and two-shot, config 5's
+    put + signal AllGather at 8 chunks per signal, and the AUTO crossover (64 / 256 KiB per rank).
+    x3: the config-3 fp32 inputs already on the host."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    oracle.build()
+    nthr = os.cpu_count() or 1
+    rows = []
+
+    def row(name, algo, dtype, R, S, ts, comp, parity, check, logical=None):
+        mean = sum(ts) / len(ts)
+        d = {"row": name, "algo": algo, "dtype": dtype, "R": R, "bytes_per_rank": S,
+             "launches": len(ts), "kernel_ms": mean, "kernel_ms_median": statistics.median(ts),
+             "bytes_model": "compulsory: every input read once, every output written once",
+             "bytes_per_launch": comp, "achieved_gbs": comp / (mean * 1e-3) / 1e9,
+             "frac": comp / (mean * 1e-3) / 1e9 / peak, "parity": bool(parity), "check": check}
+        if logical:
+            d["logical_gbs"] = logical / (mean * 1e-3) / 1e9
+        rows.append(d)
+
+    def allreduce_rows(name, x, dtype, algos):
+        R, n = x.shape
+        S = n * x.itemsize
+        send, recv = sm.Window(R, S), sm.Window(R, S)
+        try:
+            for r in range(R):
+                send.write(r, x[r])
+            stream.synchronize()
+            want, _ = oracle.allreduce_sum_mt(x, nthr)
+            y = np.empty(n, x.dtype)
+            for algo in algos:
+                ts = _time_launches(lambda: sm.sym_allreduce(send, recv, n, dtype, "sum", algo), 20,
+                                    stream)
+                if sm.sym_stream_status() != sm.SYM_OK:
+                    raise RuntimeError(f"{name} {algo}: " + sm.sym_last_error())
+                ok = True
+                for r in range(R):
+                    recv.read(r, y)
+                    stream.synchronize()
+                    ok &= bool(np.array_equal(y.view(np.uint8), want.view(np.uint8)))
+                m = algo_bytes(algo, R, S)
+                row(name, algo, dtype, R, S, ts, m["compulsory"], ok,
+                    "every element of every rank equals the oracle (bit-exact)", m["logical"])
+        finally:
+            send.free()
+            recv.free()
+
+    allreduce_rows("config3 bf16", wl.to_bf16_bits(x3), "bf16", ["twoshot", "twoshot_pull"])
+    allreduce_rows("config3 f32", x3, "f32", ["twoshot_pull"])
+    allreduce_rows("config2 f32", wl.config_inputs(2), "f32", ["oneshot", "twoshot"])
+
+    # config 5: put + signal AllGather, R=16 x 32 MiB, 64 KiB chunks, 8 chunks per signal
+    c5 = wl.PUT_SIGNAL
+    R, S, chunk, batch = c5["R"], c5["nbytes"], c5["chunk"], c5["batch"]
+    xb = wl.random_bytes(5, R, S)
+    send, recv = sm.Window(R, S, ncounters=1), sm.Window(R, R * S, nsignals=R)
+    try:
+        for r in range(R):
+            send.write(r, xb[r])
+        stream.synchronize()
+        ts = _time_launches(lambda: sm.sym_allgather(send, recv, S // 4, "f32", "put_signal", chunk,
+                                                     batch), 20, stream)
+        if sm.sym_stream_status() != sm.SYM_OK:
+            raise RuntimeError("config5: " + sm.sym_last_error())
+        want, sig, cnt = oracle.put_signal_allgather(xb, chunk, batch)
+        del xb
+        ok = True
+        out = np.empty(R * S, np.uint8)
+        for p in range(R):
+            recv.read(p, out)
+            stream.synchronize()
+            ok &= bool(np.array_equal(out, want))
+            ok &= all(sm.sym_signal_read(recv, p, q) == int(sig[p, q]) for q in range(R))
+            ok &= sm.sym_counter_read(send, p, 0) == int(cnt[p])
+        row("config5 put_signal allgather", "put_signal (64 KiB chunks, 8 per signal)", "bytes", R, S,
+            ts, R * S + R * R * S, ok,
+            "every rank's gathered bytes, all R*R signal counts and R counters equal the oracle's "
+            "sequential put + signal model")
+    finally:
+        send.free()
+        recv.free()
+
+    # AUTO crossover: device time per call from 100 calls in a CUDA graph, replayed 10 times
+    points = []
+    for nbytes in (64 << 10, 256 << 10):
+        R, n = 8, nbytes // 4
+        x = wl.config_inputs(4, n=n)
+        send, recv = sm.Window(R, nbytes), sm.Window(R, nbytes)
+        try:
+            for r in range(R):
+                send.write(r, x[r])
+            stream.synchronize()
+            pt = {"bytes_per_rank": nbytes, "auto": sm.sym_allreduce_algo(send, n, "f32")}
+            for algo in ("oneshot", "twoshot"):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for _ in range(100):
+                        sm.sym_allreduce(send, recv, n, "f32", "sum", algo)
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(10):
+                    g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                pt[f"{algo}_us"] = e0.elapsed_time(e1) * 1e3 / 1000
+                del g
+            want = oracle.allreduce_sum_f32(x)
+            sm.sym_allreduce(send, recv, n, "f32", "sum", "auto")
+            ok = sm.sym_stream_status() == sm.SYM_OK
+            y = np.empty(n, np.float32)
+            for r in range(R):
+                recv.read(r, y)
+                stream.synchronize()
+                ok &= bool(np.array_equal(y.view(np.uint32), want.view(np.uint32)))
+            pt["faster"] = "oneshot" if pt["oneshot_us"] < pt["twoshot_us"] else "twoshot"
+            pt["auto_picks_faster"] = pt["auto"] == pt["faster"]
+            pt["parity"] = bool(ok)
+            points.append(pt)
+        finally:
+            send.free()
+            recv.free()
+    rows.append({"row": "config4 AUTO crossover", "R": 8, "dtype": "f32",
+                 "threshold": "SYM_ONESHOT_MAX_BYTES (128 KiB per rank)", "points": points,
+                 "parity": all(p["parity"] for p in points),
+                 "check": "AUTO's result on every rank equals the oracle (bit-exact)"})
+    return rows
 
 
 def run_sweep(args) -> int:
@@ -757,6 +906,8 @@ def parse(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other rows (config 3 bf16, config 2, config 5, AUTO crossover)")
     ap.add_argument("--sweep", action="store_true",
                     help="message-size sweep of every algorithm instead of the contract line")
     ap.add_argument("--sweep-max", type=int, default=1 << 30)

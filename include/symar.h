@@ -203,9 +203,10 @@ sym_status_t sym_allreduce(sym_win_t send, sym_win_t recv, size_t count, sym_dty
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  All calls on a device share the array and it
- * keeps the last call's contents (flags carry a per-call epoch, the status
- * words are cleared at each call), so calls that overlap on the GPU race:
- * order them on one stream.  If a wait for another block's tile ever runs
+ * keeps the last call's contents (flags carry an epoch that the host draws
+ * for each call at the moment the call is made; the status words, which are
+ * diagnostics no call reads back, are cleared at each call), so calls that
+ * overlap on the GPU race: order them on one stream.  If a wait for another block's tile ever runs
  * out, the waiting block reduces that tile itself from the inputs, so the
  * result is still complete.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 sym_status_t sym_allreduce_noalloc(const void* send, void* recv, size_t stride, int R, size_t count,

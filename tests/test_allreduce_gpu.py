@@ -4,6 +4,8 @@ fp32: bit-exact (same rank order, IEEE adds).  bf16: within 1 ulp of the
 oracle's fp32-accumulated, once-rounded result (expected bit-exact as well;
 the exact-match count is asserted separately).
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -330,10 +332,10 @@ def test_config4_sweep(symar, oracle, nbytes):
     _full(symar, oracle, x, "f32", ALGOS + ["auto"])
 
 
-def test_config4_sweep_1gib_sampled(symar, oracle):
-    """The 1 GiB-per-rank point: sampled outputs against the oracle (computed one
-    column at a time), plus every rank's output identical on the device."""
-    import torch
+def test_config4_sweep_1gib_full(symar, oracle):
+    """The 1 GiB-per-rank point, every element of every rank against the oracle
+    ([SYMEX] Example 1 step 6 checks every element), for every algorithm and AUTO.
+    Host memory: the 8 GiB of inputs, the 1 GiB oracle result and one rank's output."""
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
     R, n = 8, (1 << 30) // 4
@@ -341,19 +343,17 @@ def test_config4_sweep_1gib_sampled(symar, oracle):
     send, recv = symar.Window(R, n * 4), symar.Window(R, n * 4)
     try:
         upload(send, x)
-        idx = np.sort(np.random.default_rng(1).choice(n, size=1 << 16, replace=False))
-        idx = np.concatenate([idx, [0, n - 1]])
-        want = oracle.allreduce_sum_f32(np.ascontiguousarray(x[:, idx]))
+        want, _ = oracle.allreduce_sum_mt(x, os.cpu_count() or 1)
         del x
-        for algo in ["oneshot", "twoshot", "twoshot_pull"]:
+        want_u = want.view(np.uint32)
+        y = np.empty(n, np.float32)
+        for algo in ["oneshot", "twoshot", "twoshot_pull", "twoshot_split", "auto"]:
             symar.sym_allreduce(send, recv, n, "f32", "sum", algo)
             assert symar.sym_stream_status() == symar.SYM_OK
-            t = recv.tensor(torch.float32)[:, :n]
-            for r in range(1, R):
-                assert torch.equal(t[0], t[r]), (algo, r)
-            got = t[0][torch.from_numpy(idx).cuda()].cpu().numpy()
-            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), algo
-            del t
+            for r in range(R):
+                recv.read(r, y)
+                sync()
+                assert np.array_equal(y.view(np.uint32), want_u), (algo, r)
             recv.tensor().zero_()
             sync()
     finally:

@@ -93,6 +93,9 @@ def test_reference_arm_prints_line():
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["metric"] == bench.METRIC
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # the same workload as the GPU arm's line, timed whole every step
+    assert d["config"] == bench._config(bench.R_DEFAULT, bench.N_DEFAULT)
+    assert "whole workload" in d["cpu_baseline"]["sample"]
 
 
 def test_reference_arm_nonzero_rank_is_silent():
