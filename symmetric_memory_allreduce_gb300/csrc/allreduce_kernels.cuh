@@ -201,6 +201,7 @@ struct ArArgs {
     int mode;                // 0 fused, 1 reduce-scatter only, 2 all-gather only
     uint32_t* status;
     uint32_t* giveup;        // give-up word of the waits (see report_timeout)
+    unsigned long long* ticket;  // work tickets of the warp-specialised pull (zeroed per launch)
     uint32_t tag;            // this launch's give-up tag (static-scratch variant)
     uint64_t timeout_ns;
 };
@@ -587,6 +588,191 @@ __global__ void __launch_bounds__(kThreads, pull_blocks_per_sm<T, Op>()) k_twosh
     if (a.tail_n && blockIdx.x == gridDim.x - 1) reduce_tail<T, Op>(a, 0, a.R);
 }
 
+// ----------------------------------------------------------------- two-shot pull, warp-specialised
+//
+// The same reduce-scatter / flag / pull all-gather, with the two phases run by
+// different warps of every CTA so that a wait for a flag never holds up a
+// reduction:
+//  * 8 reducer warps take reduce items (chunk q, 16 KiB tile t), tile-major,
+//    from the low half of the recv window's 64-bit ticket; they fold the R
+//    windows into recv_q (left in L2), meet on a named barrier, and one thread
+//    releases the tile's flag (st.release.gpu = epoch);
+//  * one copy warp, driven by its first lane, takes tiles in the same order
+//    from the ticket's high half, acquires each tile's flag (ld.acquire.gpu,
+//    bounded) and performs the pulls recv_r[tile] = recv_q[tile] for every
+//    reader r != q with the TMA engine: a bulk load into a shared-memory stage,
+//    a bulk store out of it, kWsLoads loads in flight.
+// Both halves of the ticket hand out work in index order, so the work in
+// flight is a compact range of the windows and no CTA idles while another
+// still holds a long queue.  Reducers never wait, so every flag is released as
+// long as all CTAs are resident (cooperative launch); copy lanes wait only on
+// flags of tiles some reducer has taken or will take.
+
+constexpr int kWsReducers = 256;                 // 8 reducer warps (threads 0..255)
+constexpr int kWsThreads = kWsReducers + 32;     // + the copy warp
+// The copy lane's ring: 16 KiB shared-memory stages, kWsLoads bulk loads kept in flight.
+// Measured at R = 8 x 256 MiB fp32: 3 stages / 2 loads read 12 % more DRAM than the
+// compulsory bytes (the pulls fell behind the reductions and missed L2) and reached 0.86 of
+// the copy bandwidth; 4 stages / 3 loads 0.95 (6 / 4 the same, at fewer CTAs per SM).
+constexpr int kWsStages = 4;
+constexpr int kWsLoads = kWsStages - 1;
+
+__host__ constexpr size_t ws_smem_bytes() {
+    return (size_t)kWsStages * kPullTileBytes + (size_t)kWsStages * sizeof(uint64_t);
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Generic-proxy writes made visible by an acquire -> later bulk (async-proxy) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Reduce 16 KiB tile t of chunk q into recv_q, one vector per thread and rank at a time
+// (RB ranks' loads in flight), four steps of kWsReducers vectors.
+template <class T, class Op, int RB>
+__device__ __forceinline__ void ws_reduce_tile(const ArArgs& a, uint32_t q, uint32_t t) {
+    constexpr size_t TILEV = (size_t)kWsReducers * kPullU;
+    const size_t c0 = (size_t)q * a.chunk_vec;
+    const size_t c1 = min(c0 + a.chunk_vec, a.nvec);
+    const size_t v0 = c0 + (size_t)t * TILEV;
+    char* dst = a.recv + (size_t)q * a.rstride;
+#pragma unroll 1
+    for (int h = 0; h < kPullU; ++h) {
+        size_t idx[1] = {v0 + threadIdx.x + (size_t)h * kWsReducers};
+        bool ok[1] = {idx[0] < c1};
+        if (!__any_sync(0xffffffffu, ok[0])) break;        // the rest of the tile is past the chunk
+        float acc[1][T::V];
+        reduce_vectors<T, Op, RB, 1, kLoadStream>(a.send, a.sstride, a.R, idx, ok, acc);
+        if (ok[0]) store16_keep(dst + idx[0] * kVecBytes, T::narrow(acc[0]));
+    }
+}
+
+// resident CTAs per SM: the copy lane's 64 KiB ring allows three, so the
+// register budget is set for three (no spills for any element type)
+template <class T>
+constexpr int ws_blocks_per_sm() {
+    return 3;
+}
+
+template <class T, class Op, int RB>
+__global__ void __launch_bounds__(kWsThreads, ws_blocks_per_sm<T>()) k_twoshot_pull_ws(ArArgs a) {
+    extern __shared__ __align__(128) unsigned char ws_smem[];
+    __shared__ uint32_t s_item[2];
+    constexpr size_t TILEV = (size_t)kWsReducers * kPullU;
+    const uint32_t R = (uint32_t)a.R, T_ = a.tiles_per_chunk;
+    const uint32_t items = R * T_;                              // tiles, i = t * R + q
+    const uint32_t ep = read_epoch(a.epoch_ptr);                // every thread: has a barrier
+    auto tile_range = [&](uint32_t i, uint32_t& q, uint32_t& t, size_t& v0, size_t& v1) {
+        t = i / R;
+        q = i - t * R;
+        const size_t c0 = (size_t)q * a.chunk_vec;
+        const size_t c1 = min(c0 + a.chunk_vec, a.nvec);
+        v0 = c0 + (size_t)t * TILEV;
+        v1 = min(v0 + TILEV, c1);
+        if (v1 < v0) v1 = v0;
+    };
+    if (threadIdx.x < kWsReducers) {
+        // reduce items from the ticket's low half; the next item is fetched before the
+        // barrier that ends the current one (two slots: readers of one never race the writer)
+        int par = 0;
+        if (threadIdx.x == 0) s_item[0] = (uint32_t)atomicAdd(a.ticket, 1ull);
+        named_barrier_sync(1, kWsReducers);
+        uint32_t i = s_item[0];
+        while (i < items) {
+            uint32_t q, t;
+            size_t v0, v1;
+            tile_range(i, q, t, v0, v1);
+            if (v0 < v1) ws_reduce_tile<T, Op, RB>(a, q, t);
+            if (threadIdx.x == 0) s_item[par ^ 1] = (uint32_t)atomicAdd(a.ticket, 1ull);
+            named_barrier_sync(1, kWsReducers);                 // the tile is stored
+            // one release after the barrier publishes every reducer thread's stores
+            if (threadIdx.x == 0 && v0 < v1) st_release_u32(a.flags + (size_t)q * a.flag_stride + t, ep);
+            par ^= 1;
+            i = s_item[par];
+        }
+        if (a.tail_n && blockIdx.x == gridDim.x - 1) reduce_tail<T, Op>(a, 0, a.R);
+        return;
+    }
+    if (threadIdx.x != kWsReducers || R < 2) return;           // lane 0 of the copy warp drives
+    uint64_t* bar = reinterpret_cast<uint64_t*>(ws_smem + (size_t)kWsStages * kPullTileBytes);
+    for (int s = 0; s < kWsStages; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+    bool alive = true;                   // false once a flag wait ran out: issue nothing more
+    // the copies: for every tile taken from the ticket's high half, one per reader r != q
+    uint32_t cur_i = 0, cur_j = R - 1;   // tile being split into copies, next reader index
+    struct Copy {
+        uint32_t q, t, r, bytes;
+        size_t off;
+    };
+    auto next_copy = [&](Copy& c) {
+        while (cur_j == R - 1) {                                // take the next non-empty tile
+            cur_i = (uint32_t)(atomicAdd(a.ticket, 1ull << 32) >> 32);
+            if (cur_i >= items) return false;
+            uint32_t q, t;
+            size_t v0, v1;
+            tile_range(cur_i, q, t, v0, v1);
+            if (v0 < v1) cur_j = 0;
+        }
+        size_t v0, v1;
+        tile_range(cur_i, c.q, c.t, v0, v1);
+        c.r = cur_j < c.q ? cur_j : cur_j + 1;
+        c.off = v0 * kVecBytes;
+        c.bytes = (uint32_t)((v1 - v0) * kVecBytes);
+        if (cur_j == 0 && alive) {                              // first copy of the tile: acquire
+            const uint32_t* f = a.flags + (size_t)c.q * a.flag_stride + c.t;
+            alive = bounded_spin([&] { return ld_acquire_u32(f) == ep; }, a.timeout_ns, a.giveup, ep);
+            if (!alive) report_timeout(a.status, a.giveup, ep, kSitePullFlag, c.q, c.t);
+            fence_proxy_async_global();
+        }
+        ++cur_j;
+        return true;
+    };
+    auto issue_load = [&](const Copy& c, int s) {
+        const uint32_t bytes = alive ? c.bytes : 0u;
+        mbar_expect_tx(&bar[s], bytes);
+        if (bytes)
+            bulk_load(ws_smem + (size_t)s * kPullTileBytes, a.recv + (size_t)c.q * a.rstride + c.off,
+                      bytes, &bar[s]);
+    };
+    Copy ring[kWsStages];
+    uint64_t issued = 0, done = 0;
+    while (issued < (uint64_t)kWsLoads && next_copy(ring[issued % kWsStages])) {
+        issue_load(ring[issued % kWsStages], (int)(issued % kWsStages));
+        ++issued;
+    }
+    while (done < issued) {
+        const int s = (int)(done % kWsStages);
+        const uint32_t parity = (uint32_t)((done / kWsStages) & 1u);
+        uint32_t spins = 0;
+        while (!mbar_try_wait(&bar[s], parity)) {
+            if (++spins > (1u << 26)) {                         // a bulk load never fails; bounded anyway
+                report_timeout(a.status, a.giveup, ep, kSiteBulkStage, blockIdx.x, (uint32_t)done);
+                bulk_wait_all<0>();
+                return;
+            }
+        }
+        const Copy& c = ring[s];
+        if (alive && c.bytes)
+            bulk_store(a.recv + (size_t)c.r * a.rstride + c.off, ws_smem + (size_t)s * kPullTileBytes,
+                       c.bytes);
+        bulk_commit();
+        ++done;
+        Copy n;
+        if (next_copy(n)) {
+            // stage issued % stages was last read by the store of copy issued - stages,
+            // committed before the one just committed
+            bulk_wait_read<kWsStages - kWsLoads>();
+            ring[issued % kWsStages] = n;
+            issue_load(n, (int)(issued % kWsStages));
+            ++issued;
+        }
+    }
+    bulk_wait_all<0>();
+}
+
 // ----------------------------------------------------------------- host launcher
 
 
@@ -665,12 +851,28 @@ sym_status_t launch_algo(sym_algo_t algo, ArArgs& a, sym_win_t recv, cudaStream_
             }
             // fused: blocks wait on one another -> co-residency via a cooperative launch
             {
-                sym_status_t s = bump_epoch(recv->epoch, st);
+                // the warp-specialised kernel takes its work from the window's ticket
+                sym_status_t s = bump_epoch(recv->epoch, st, pull_use_ws() ? recv->ticket : nullptr);
                 if (s != SYM_OK) return s;
             }
             a.epoch_ptr = recv->epoch;
             a.giveup = recv->giveup;
+            a.ticket = recv->ticket;
             a.mode = 0;
+            if (pull_use_ws()) {
+                void (*kws)(ArArgs) = k_twoshot_pull_ws<T, Op, 8>;
+                const size_t smem = ws_smem_bytes();
+                SYM_CUDA(cudaFuncSetAttribute((const void*)kws,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+                const int occ_ws = occupancy((const void*)kws, kWsThreads, smem);
+                const size_t items = std::max((size_t)a.R * a.tiles_per_chunk, (size_t)1);
+                const size_t grid = std::min(items, (size_t)std::max(occ_ws, 1) * sms);
+                void* args[] = {&a};
+                SYM_CUDA(cudaLaunchCooperativeKernel((const void*)kws, dim3((unsigned)grid),
+                                                     dim3(kWsThreads), args, smem, st));
+                count_launch();
+                break;
+            }
             // two 16 KiB tiles per item, gathers 4 grid waves behind: measured best
             // of 1/2/4/8 tiles x 2/4/8 waves (config 3 fp32 0.721 -> 0.685 ms)
             a.group = kPullGroup;

@@ -8,6 +8,7 @@
 // live in one allocation at base + r*stride ([LSA] "base plus offset"), so a
 // peer address is pure integer arithmetic and every kernel can reach every
 // rank with ordinary loads and stores.
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
@@ -123,6 +124,14 @@ bool twoshot_use_bulk() {
     static const bool v = [] {
         const char* s = getenv("SYM_TWOSHOT_KERNEL");
         return s && strcmp(s, "bulk") == 0;
+    }();
+    return v;
+}
+
+bool pull_use_ws() {
+    static const bool v = [] {
+        const char* s = getenv("SYM_PULL_KERNEL");
+        return !(s && strcmp(s, "items") == 0);
     }();
     return v;
 }
