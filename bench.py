@@ -893,6 +893,185 @@ def run_suite(args) -> int:
     return 0
 
 
+# ----------------------------------------------------------------- results table
+
+# kernel-name patterns of each row's main launch, for matching an ncu launch list to the rows
+_MAIN_KERNEL = {"oneshot": "k_oneshot", "twoshot": "k_twoshot_st", "twoshot_pull": "k_twoshot_pull_ws",
+                "put_signal": "k_put_signal_allgather"}
+
+
+def table_rows():
+    """(label, config index, algo, dtype, count or bytes, extra) of every results-table row."""
+    rows = []
+    for dist in ("rankfill", "normal"):
+        for algo in ("oneshot", "twoshot"):
+            rows.append((f"1 ({'rank fill' if dist == 'rankfill' else 'N(0,1)'})", 1, algo, "f32",
+                         1 << 20, dist))
+    for algo in ("oneshot", "twoshot", "twoshot_pull"):
+        rows.append(("2", 2, algo, "f32", 1 << 24, None))
+    for dt in ("f32", "bf16"):
+        for algo in ("twoshot", "twoshot_pull"):
+            rows.append(("3", 3, algo, dt, 1 << 26, None))
+    for k in range(11):
+        nbytes = 1024 * 4 ** k
+        size = f"{nbytes >> 10} KiB" if nbytes < (1 << 20) else (
+            f"{nbytes >> 20} MiB" if nbytes < (1 << 30) else f"{nbytes >> 30} GiB")
+        for algo in ("oneshot", "twoshot"):
+            rows.append((f"4: {size}/rank", 4, algo, "f32", nbytes // 4, None))
+    for batch in (8, 1, 64):
+        rows.append((f"5 (64 KiB chunks, {batch}/signal)", 5, "put_signal", "bytes", 32 << 20, batch))
+    return rows
+
+
+def _table_inputs(cfg, dt, n, extra):
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    if cfg == 5:
+        return wl.random_bytes(5, wl.PUT_SIGNAL["R"], n)
+    x = wl.config_inputs(cfg, n=n, dist=extra) if cfg != 4 else wl.config_inputs(4, n=n)
+    return wl.to_bf16_bits(x) if dt == "bf16" else x
+
+
+def parse_dram_csv(path: str) -> list[tuple[str, float]]:
+    """(kernel name, DRAM bytes read + written) of every launch in an ncu --csv launch list."""
+    import csv
+
+    per = {}
+    order = []
+    with open(path) as f:
+        lines = [l for l in f if l.startswith('"')]
+    for rec in csv.DictReader(lines):
+        key = rec.get("ID")
+        if key not in per:
+            per[key] = [rec.get("Kernel Name", ""), 0.0]
+            order.append(key)
+        if rec.get("Metric Name") in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            v = float(rec["Metric Value"].replace(",", ""))
+            unit = rec.get("Metric Unit", "byte")
+            scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(unit, 1)
+            per[key][1] += v * scale
+    return [(per[k][0], per[k][1]) for k in order]
+
+
+def run_table(args) -> int:
+    """The benchmark results table: every config x algo x dtype row timed (CUDA events, >= 20
+    launches and >= 200 ms after 5 warm-ups), every rank's output compared with the oracle, the
+    oracle timed on 1 and on all host threads.  --table-dram-pass instead launches each row's call
+    once (run it under ncu with the one-pass DRAM metrics); --dram-csv reads that launch list back
+    into the table's DRAM column.  Markdown on stdout."""
+    import numpy as np
+    import torch
+
+    import symmetric_memory_allreduce_gb300 as sm
+    from symmetric_memory_allreduce_gb300 import workloads as wl
+
+    torch.cuda.set_device(0)
+    sm.load()
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peak()
+    dram = parse_dram_csv(args.dram_csv) if args.dram_csv else None
+    dram_pos = 0
+    nthr = os.cpu_count() or 1
+    out = []
+    if not args.table_dram_pass:
+        import oracle
+
+        oracle.build()
+    for label, cfg, algo, dt, n, extra in table_rows():
+        x = _table_inputs(cfg, dt, n, extra)
+        R = x.shape[0]
+        if cfg == 5:
+            S = x.shape[1]
+            c5 = wl.PUT_SIGNAL
+            send, recv = sm.Window(R, S, ncounters=1), sm.Window(R, R * S, nsignals=R)
+            call = (lambda: sm.sym_allgather(send, recv, S // 4, "f32", "put_signal", c5["chunk"], extra))
+            comp, logical = R * S + R * R * S, 2 * R * R * S
+        else:
+            S = x.shape[1] * x.itemsize
+            send, recv = sm.Window(R, S), sm.Window(R, S)
+            call = (lambda: sm.sym_allreduce(send, recv, x.shape[1], dt, "sum", algo))
+            m = algo_bytes(algo, R, S)
+            comp, logical = m["compulsory"], m["logical"]
+        try:
+            for r in range(R):
+                send.write(r, x[r])
+            stream.synchronize()
+            if args.table_dram_pass:
+                call()
+                torch.cuda.synchronize()
+                continue
+            iters = max(20, min(2000, int(4e9 / max(comp, 1))))
+            ts = _time_launches(call, iters, stream, None, 200.0)
+            if sm.sym_stream_status() != sm.SYM_OK:
+                raise RuntimeError(f"{label} {algo}: " + sm.sym_last_error())
+            med = statistics.median(ts)
+            # parity: every rank's output against the oracle; oracle timed on 1 and nthr threads
+            if cfg == 5:
+                t0 = time.perf_counter()
+                want, sig, cnt = oracle.put_signal_allgather(x, wl.PUT_SIGNAL["chunk"], extra)
+                t1_ms, tn_ms = (time.perf_counter() - t0) * 1e3, None
+                ok = True
+                buf = np.empty(R * S, np.uint8)
+                for p in range(R):
+                    recv.read(p, buf)
+                    stream.synchronize()
+                    ok &= bool(np.array_equal(buf, want))
+                    ok &= all(sm.sym_signal_read(recv, p, q) == int(sig[p, q]) for q in range(R))
+                    ok &= sm.sym_counter_read(send, p, 0) == int(cnt[p])
+            else:
+                t0 = time.perf_counter()
+                oracle.allreduce_sum_mt(x, 1)
+                t1_ms = (time.perf_counter() - t0) * 1e3
+                t0 = time.perf_counter()
+                want, _ = oracle.allreduce_sum_mt(x, nthr)
+                tn_ms = (time.perf_counter() - t0) * 1e3
+                ok = True
+                y = np.empty(x.shape[1], x.dtype)
+                for r in range(R):
+                    recv.read(r, y)
+                    stream.synchronize()
+                    ok &= bool(np.array_equal(y.view(np.uint8), want.view(np.uint8)))
+            row = {"label": label, "algo": algo, "dtype": dt, "R": R, "bytes_per_rank": S,
+                   "t_ms": med, "launches": len(ts), "algbw": S / (med * 1e-3) / 1e9,
+                   "logical_gbs": logical / (med * 1e-3) / 1e9,
+                   "compulsory_gbs": comp / (med * 1e-3) / 1e9, "parity": ok,
+                   "oracle_1t_ms": t1_ms, "oracle_nt_ms": tn_ms, "l2_resident": 2 * R * S < (126 << 20)}
+            if dram is not None:
+                pat = _MAIN_KERNEL[algo]
+                while dram_pos < len(dram) and pat not in dram[dram_pos][0]:
+                    dram_pos += 1
+                if dram_pos < len(dram):
+                    row["dram_bytes"] = dram[dram_pos][1]
+                    row["dram_gbs"] = dram[dram_pos][1] / (med * 1e-3) / 1e9
+                    dram_pos += 1
+            out.append(row)
+            print(json.dumps(row), file=sys.stderr, flush=True)
+        finally:
+            send.free()
+            recv.free()
+    if args.table_dram_pass:
+        return 0
+    print(f"| Config | Algo | dtype | t median (ms) | algbw GB/s | logical GB/s | compulsory GB/s "
+          f"| HBM GB/s (ncu DRAM bytes / t) | % of measured peak | parity | oracle 1-thread (ms) "
+          f"| oracle {nthr}-thread (ms) |")
+    print("|---|---|---|---|---|---|---|---|---|---|---|---|")
+    for r in out:
+        if "dram_gbs" in r:
+            hbm = f"{r['dram_gbs']:,.0f}"
+            pct = ("L2-resident (n/m)" if r["l2_resident"] else f"{100 * r['dram_gbs'] / peak:.1f} %")
+        else:
+            hbm, pct = "—", ("L2-resident (n/m)" if r["l2_resident"] else
+                             f"{100 * r['compulsory_gbs'] / peak:.1f} % (compulsory)")
+        parity = "bit-exact" if r["parity"] else "**MISMATCH**"
+        tn = f"{r['oracle_nt_ms']:.1f}" if r["oracle_nt_ms"] is not None else "—"
+        print(f"| {r['label']} | {r['algo']} | {r['dtype']} | {r['t_ms']:.4f} | {r['algbw']:,.1f} "
+              f"| {r['logical_gbs']:,.0f} | {r['compulsory_gbs']:,.0f} | {hbm} | {pct} | {parity} "
+              f"| {r['oracle_1t_ms']:.1f} | {tn} |")
+    print(f"\nPeak: {peak:,.0f} GB/s ({peak_kind} HBM copy bandwidth, MEASURED_PEAKS.json); "
+          f"host: {cpu_model()}, {nthr} threads.")
+    return 0
+
+
 def parse(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -922,6 +1101,12 @@ def parse(argv=None):
                     help="--suite: divide every per-rank size by this (small profiling cases)")
     ap.add_argument("--suite-iters", type=int, default=0,
                     help="--suite: timed launches per row (0: by size); small for profiler runs")
+    ap.add_argument("--table", action="store_true",
+                    help="the results table (every config x algo x dtype) as markdown")
+    ap.add_argument("--table-dram-pass", action="store_true",
+                    help="--table: launch each row's call once (for an ncu one-pass DRAM launch list)")
+    ap.add_argument("--dram-csv", default="",
+                    help="--table: ncu --csv launch list of a --table-dram-pass run (DRAM column)")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)          # at least three untimed warm-up steps
     return a
@@ -935,6 +1120,8 @@ def main(argv=None) -> int:
         return run_sweep(args)
     if args.suite:
         return run_suite(args)
+    if args.table or args.table_dram_pass:
+        return run_table(args)
     return run_ours(args)
 
 
