@@ -114,7 +114,9 @@ size_t oneshot_max_bytes();
 bool twoshot_use_bulk();          // env SYM_TWOSHOT_KERNEL=bulk|ldst
 bool allgather_use_bulk();        // env SYM_ALLGATHER_KERNEL=bulk (default)|ldst
 bool put_use_bulk();              // env SYM_PUT_KERNEL=bulk (default)|ldst
-bool pull_use_ws();               // env SYM_PULL_KERNEL=ws (default)|items
+// Fused pull two-shot kernel for `bytes` per rank: env SYM_PULL_KERNEL=ws (warp-specialised),
+// items (single-role), or auto (default: ws above 256 KiB per rank).
+bool pull_use_ws(size_t bytes);
 // Grid waves between a tile's producing item and the items that wait for it
 // (fused pull two-shot); env SYM_PULL_LAG_WAVES, default 4, 1..64.
 uint32_t pull_lag_waves();

@@ -128,12 +128,14 @@ bool twoshot_use_bulk() {
     return v;
 }
 
-bool pull_use_ws() {
-    static const bool v = [] {
+bool pull_use_ws(size_t bytes) {
+    static const int mode = [] {          // 0 auto, 1 ws, 2 items
         const char* s = getenv("SYM_PULL_KERNEL");
-        return !(s && strcmp(s, "items") == 0);
+        if (s && strcmp(s, "ws") == 0) return 1;
+        if (s && strcmp(s, "items") == 0) return 2;
+        return 0;
     }();
-    return v;
+    return mode == 1 || (mode == 0 && bytes > (size_t)256 * 1024);
 }
 
 int64_t fused_lag_blocks() {
