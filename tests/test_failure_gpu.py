@@ -110,3 +110,55 @@ def test_dropped_first_signal_stops_the_stream_in_order():
     assert out.returncode == 0, out.stdout[-3000:] + out.stderr[-3000:]
     assert "FAILURE_TEST_OK" in out.stdout
     assert "site 6" in out.stdout          # the batch-order wait reported it
+
+
+_PULL_GIVE_UP = r"""
+import sys, time
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import numpy as np
+import oracle
+import symmetric_memory_allreduce_gb300 as sm
+from _gpu_util import upload, download
+sm.load(); oracle.build()
+for R, n in ((8, 1 << 22), (8, 40_000)):       # the warp-specialised kernel, then the single-role one
+    x = np.random.default_rng(n).standard_normal((R, n)).astype(np.float32)
+    want = oracle.allreduce_sum_f32(x)
+    a, b = sm.Window(R, n * 4), sm.Window(R, n * 4)
+    upload(a, x)
+    t0 = time.time()
+    sm.sym_allreduce(a, b, n, "f32", "sum", "twoshot_pull")
+    st = sm.sym_stream_status()
+    dt = time.time() - t0
+    print("N", n, "STATUS", sm.sym_status_string(st), "SECONDS", round(dt, 3), "WHERE", sm.sym_last_error())
+    assert dt < 10.0
+    y = download(b, n * 4, np.float32)
+    if st == sm.SYM_OK:
+        assert all(np.array_equal(y[r].view(np.uint32), want.view(np.uint32)) for r in range(R))
+    else:
+        assert st == sm.SYM_ERR_TIMEOUT and "site 3" in sm.sym_last_error()
+        # reducers never wait: every slot's own chunk is complete even when pulls gave up
+        nvec = n * 4 // 16
+        cv = -(-nvec // R) * 4
+        for q in range(R):
+            lo, hi = q * cv, min((q + 1) * cv, nvec * 4)
+            assert np.array_equal(y[q, lo:hi].view(np.uint32), want[lo:hi].view(np.uint32)), q
+    # the context stays usable: the store-form two-shot (no waits) afterwards is exact
+    sm.sym_allreduce(a, b, n, "f32", "sum", "twoshot")
+    assert sm.sym_stream_status() == sm.SYM_OK
+    y = download(b, n * 4, np.float32)
+    assert all(np.array_equal(y[r].view(np.uint32), want.view(np.uint32)) for r in range(R))
+    a.free(); b.free()
+print("PULL_GIVE_UP_OK")
+"""
+
+
+def test_pull_waits_give_up_cleanly():
+    """Pull two-shot with every flag wait bounded at 1 ns: pulls that find their tile's flag
+    unset give up (the launch ends, SYM_ERR_TIMEOUT at the pull-flag site), the slots' own
+    reduced chunks are still exact, and the context stays usable."""
+    env = dict(os.environ, SYM_TIMEOUT_NS="1")
+    out = subprocess.run([sys.executable, "-c", _PULL_GIVE_UP.format(root=ROOT,
+                                                                     tests=os.path.join(ROOT, "tests"))],
+                         env=env, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stdout[-3000:] + out.stderr[-3000:]
+    assert "PULL_GIVE_UP_OK" in out.stdout
