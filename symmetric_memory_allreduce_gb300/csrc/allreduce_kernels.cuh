@@ -673,13 +673,10 @@ __device__ __forceinline__ void ws_reduce_tile(const ArArgs& a, uint32_t q, uint
 
 // resident CTAs per SM: the copy lane's 64 KiB ring allows three, so the
 // register budget is set for three (no spills for any element type)
-template <class T>
-constexpr int ws_blocks_per_sm() {
-    return 3;
-}
+constexpr int kWsBlocksPerSm = 3;
 
 template <class T, class Op, int RB>
-__global__ void __launch_bounds__(kWsThreads, ws_blocks_per_sm<T>()) k_twoshot_pull_ws(ArArgs a) {
+__global__ void __launch_bounds__(kWsThreads, kWsBlocksPerSm) k_twoshot_pull_ws(ArArgs a) {
     extern __shared__ __align__(128) unsigned char ws_smem[];
     __shared__ uint32_t s_item[2];
     constexpr size_t TILEV = (size_t)kWsReducers * kPullU;
