@@ -104,3 +104,34 @@ def test_reference_arm_nonzero_rank_is_silent():
                           "--steps", "2", "--warmup", "3"], env=env, capture_output=True, text=True,
                          timeout=120)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_parse_dram_csv(tmp_path):
+    """ncu --csv launch lists: per launch, dram read + write bytes summed, in launch order."""
+    p = tmp_path / "l.csv"
+    hdr = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",'
+           '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n')
+    rows = []
+    for i, (name, rd, wr) in enumerate([("k_bump_epoch(unsigned int *)", 64, 0),
+                                        ("void k_twoshot_st<F32T, OpSum, 8, 1>(ArArgs)", 1000, 900),
+                                        ("void k_oneshot<F32T, OpSum, 8, 2>(ArArgs)", 10, 20)]):
+        for metric, v in (("dram__bytes_read.sum", rd), ("dram__bytes_write.sum", wr)):
+            rows.append(f'"{i}","1","python3","h","{name}","1","7","(256, 1, 1)","(1, 1, 1)","0","10.3",'
+                        f'"Command line profiler metrics","{metric}","byte","{v}"\n')
+    p.write_text("==PROF== Connected\n" + hdr + "".join(rows))
+    got = bench.parse_dram_csv(str(p))
+    assert [n.split("<")[0].split("(")[0].split()[-1] for n, _ in got] == [
+        "k_bump_epoch", "k_twoshot_st", "k_oneshot"]
+    assert [b for _, b in got] == [64.0, 1900.0, 30.0]
+
+
+def test_table_rows_cover_every_config():
+    rows = bench.table_rows()
+    labels = {r[1] for r in rows}
+    assert labels == {1, 2, 3, 4, 5}
+    assert len({(r[0], r[2], r[3]) for r in rows}) == len(rows)          # no duplicate row
+    sweep = [r for r in rows if r[1] == 4]
+    assert sorted({r[4] * 4 for r in sweep}) == [1024 * 4 ** k for k in range(11)]
+    assert {r[2] for r in rows if r[1] == 3} == {"twoshot", "twoshot_pull"}
+    assert {r[5] for r in rows if r[1] == 5} == {1, 8, 64}
+    assert set(bench._MAIN_KERNEL) >= {r[2] for r in rows}
