@@ -10,7 +10,8 @@ HBM).  Prints ONE JSON line (rank 0):
              (read R*S + write R*S) / its average CUDA-event duration, against
              the measured copy bandwidth; traffic = ncu DRAM bytes per launch
   e2e        the same metric through the C ABI with pinned HOST buffers: every
-             step copies the R inputs in and the R results out
+             step copies the R inputs in and the result (the reduced vector every
+             rank holds, read from rank 0's window) out
   cpu_baseline  the CPU oracle (test infrastructure) timed on a bounded sample
 
   --impl reference  times the CPU oracle as the reference arm (rank 0 only).
@@ -386,9 +387,10 @@ def run_ours(args) -> int:
 
     # e2e: pinned host buffers through the C ABI, copies inside the timed region.
     # Every step copies its R inputs host -> device (sym_window_write), runs the
-    # AllReduce, and copies all R results device -> host (sym_window_read).  Two
-    # window pairs and three streams let step k+1's inputs cross the host link
-    # while step k's results come back.
+    # AllReduce, and copies the result device -> host (sym_window_read of rank
+    # 0's window: every rank holds the same reduced vector, which the oracle
+    # produces once).  Two window pairs and three streams let step k+1's inputs
+    # cross the host link while step k's result comes back.
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(sm, send, recv, x, R, n, args, world, stream)
@@ -437,10 +439,12 @@ def run_e2e(sm, send, recv, x, R, n, args, world, stream) -> dict:
     import torch
 
     S = n * 4
-    steps = max(3, min(args.steps, args.e2e_steps))
+    steps = max(3, args.e2e_steps)
     h_in = torch.empty((R, S), dtype=torch.uint8, pin_memory=True)
     h_in.numpy()[:] = x.view(np.uint8)
-    h_out = [torch.empty((R, S), dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    # the step's result: the reduced vector (every rank's window holds the same bytes; the oracle
+    # produces it once), read back from rank 0's window
+    h_out = [torch.empty((S,), dtype=torch.uint8, pin_memory=True) for _ in range(2)]
     sends = [send, sm.Window(R, S)]
     recvs = [recv, sm.Window(R, S)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
@@ -461,8 +465,7 @@ def run_e2e(sm, send, recv, x, R, n, args, world, stream) -> dict:
         sm.sym_allreduce(sends[b], recvs[b], n, "f32", "sum", args.algo, stream=stream)
         ev_done[b].record(stream)
         s_out.wait_event(ev_done[b])
-        for r in range(R):
-            recvs[b].read(r, (h_out[b].data_ptr() + r * S, S), stream=s_out)
+        recvs[b].read(0, (h_out[b].data_ptr(), S), stream=s_out)
         ev_out[b].record(s_out)
 
     for k in range(2):                              # warm-up
@@ -483,13 +486,16 @@ def run_e2e(sm, send, recv, x, R, n, args, world, stream) -> dict:
     if sm.sym_stream_status() != sm.SYM_OK:
         raise RuntimeError("e2e reported a device status: " + sm.sym_last_error())
     e_ms = max_over_ranks(e0.elapsed_time(e1)) / steps
+    # the result that came back equals the device result of the last step (bytes)
+    check = bool(torch.equal(h_out[(steps - 1) % 2], recvs[(steps - 1) % 2].tensor()[0, :S].cpu()))
     for w in (sends[1], recvs[1]):
         w.free()
     return {"value": world * S / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
-            "h2d_bytes_per_step": R * S, "d2h_bytes_per_step": R * S, "steps": steps,
+            "h2d_bytes_per_step": R * S, "d2h_bytes_per_step": S, "steps": steps,
             "ms_per_step": e_ms,
-            "host_link_gbs": 2 * R * S / (e_ms * 1e-3) / 1e9,
-            "pipeline": "2 window pairs, 3 streams: copy-in || AllReduce || copy-out"}
+            "host_link_gbs": (R * S + S) / (e_ms * 1e-3) / 1e9, "result_read_back_matches": check,
+            "pipeline": "2 window pairs, 3 streams: copy-in of the R inputs || AllReduce || "
+                        "copy-out of the result (rank 0's window)"}
 
 
 def run_secondary(sm, stream, x3, peak) -> list[dict]:
