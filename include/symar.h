@@ -384,7 +384,9 @@ sym_status_t sym_counter_reset(sym_win_t w, int rank, uint32_t counter_id, sym_s
 /* Synchronise `stream`, then report and clear the current device's status
  * word: SYM_ERR_TIMEOUT if a bounded device wait of this library ran out
  * since the last call, SYM_ERR_CUDA on a CUDA error, else SYM_OK.  [GIN] the
- * barrier's timeoutCycles overload (a wait that gives up instead of hanging). */
+ * barrier's timeoutCycles overload (a wait that gives up instead of hanging).
+ * sym_allreduce_noalloc's waits are not reported here: a gather of that entry
+ * that gives up reduces its tile itself, so its result is complete anyway. */
 sym_status_t sym_stream_status(sym_stream_t stream);
 
 const char* sym_status_string(sym_status_t s);
