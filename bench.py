@@ -1041,7 +1041,8 @@ def run_table(args) -> int:
                    "t_ms": med, "launches": len(ts), "algbw": S / (med * 1e-3) / 1e9,
                    "logical_gbs": logical / (med * 1e-3) / 1e9,
                    "compulsory_gbs": comp / (med * 1e-3) / 1e9, "parity": ok,
-                   "oracle_1t_ms": t1_ms, "oracle_nt_ms": tn_ms, "l2_resident": 2 * R * S < (126 << 20)}
+                   "oracle_1t_ms": t1_ms, "oracle_nt_ms": tn_ms, "l2_resident": 2 * R * S < (126 << 20),
+                   "oracle_threads": nthr, "cpu_model": cpu_model()}
             if dram is not None:
                 pat = _MAIN_KERNEL[algo]
                 while dram_pos < len(dram) and pat not in dram[dram_pos][0]:
@@ -1057,24 +1058,47 @@ def run_table(args) -> int:
             recv.free()
     if args.table_dram_pass:
         return 0
-    print(f"| Config | Algo | dtype | t median (ms) | algbw GB/s | logical GB/s | compulsory GB/s "
-          f"| HBM GB/s (ncu DRAM bytes / t) | % of measured peak | parity | oracle 1-thread (ms) "
-          f"| oracle {nthr}-thread (ms) |")
-    print("|---|---|---|---|---|---|---|---|---|---|---|---|")
-    for r in out:
+    print(format_table(out, peak, peak_kind, nthr, cpu_model()))
+    return 0
+
+
+def format_table(rows: list[dict], peak: float, peak_kind: str, nthr: int, cpu: str) -> str:
+    """Markdown of the results table from its JSON rows (as run_table writes them to stderr).
+    A row is flagged L2-served when its logical bytes exceed the DRAM bytes by more than 10 %:
+    repeated reads of the same lines came from L2, not HBM."""
+    lines = [f"| Config | Algo | dtype | t median (ms) | algbw GB/s | logical GB/s | compulsory GB/s "
+             f"| HBM GB/s (ncu DRAM bytes / t) | % of measured peak | logical / DRAM | parity "
+             f"| oracle 1-thread (ms) | oracle {nthr}-thread (ms) |",
+             "|---|---|---|---|---|---|---|---|---|---|---|---|---|"]
+    for r in rows:
+        ratio = "—"
         if "dram_gbs" in r:
             hbm = f"{r['dram_gbs']:,.0f}"
             pct = ("L2-resident (n/m)" if r["l2_resident"] else f"{100 * r['dram_gbs'] / peak:.1f} %")
+            if not r["l2_resident"]:
+                q = r["logical_gbs"] / r["dram_gbs"]
+                ratio = f"{q:.2f}" + (" (L2-served)" if q > 1.1 else "")
         else:
             hbm, pct = "—", ("L2-resident (n/m)" if r["l2_resident"] else
                              f"{100 * r['compulsory_gbs'] / peak:.1f} % (compulsory)")
         parity = "bit-exact" if r["parity"] else "**MISMATCH**"
         tn = f"{r['oracle_nt_ms']:.1f}" if r["oracle_nt_ms"] is not None else "—"
-        print(f"| {r['label']} | {r['algo']} | {r['dtype']} | {r['t_ms']:.4f} | {r['algbw']:,.1f} "
-              f"| {r['logical_gbs']:,.0f} | {r['compulsory_gbs']:,.0f} | {hbm} | {pct} | {parity} "
-              f"| {r['oracle_1t_ms']:.1f} | {tn} |")
-    print(f"\nPeak: {peak:,.0f} GB/s ({peak_kind} HBM copy bandwidth, MEASURED_PEAKS.json); "
-          f"host: {cpu_model()}, {nthr} threads.")
+        lines.append(f"| {r['label']} | {r['algo']} | {r['dtype']} | {r['t_ms']:.4f} | {r['algbw']:,.1f} "
+                     f"| {r['logical_gbs']:,.0f} | {r['compulsory_gbs']:,.0f} | {hbm} | {pct} | {ratio} "
+                     f"| {parity} | {r['oracle_1t_ms']:.1f} | {tn} |")
+    lines.append(f"\nPeak: {peak:,.0f} GB/s ({peak_kind} HBM copy bandwidth, MEASURED_PEAKS.json); "
+                 f"host: {cpu}, {nthr} threads.")
+    return "\n".join(lines)
+
+
+def run_table_from_json(args) -> int:
+    """Re-render the results table from the JSON rows a --table run wrote (no GPU); the host's
+    thread count and CPU come from the rows, else from --table-threads / --table-cpu."""
+    rows = [json.loads(l) for l in open(args.table_from_json) if l.startswith("{")]
+    peak, peak_kind = measured_peak()
+    nthr = rows[0].get("oracle_threads", args.table_threads) if rows else args.table_threads
+    cpu = rows[0].get("cpu_model", args.table_cpu) if rows else args.table_cpu
+    print(format_table(rows, peak, peak_kind, nthr, cpu))
     return 0
 
 
@@ -1113,6 +1137,12 @@ def parse(argv=None):
                     help="--table: launch each row's call once (for an ncu one-pass DRAM launch list)")
     ap.add_argument("--dram-csv", default="",
                     help="--table: ncu --csv launch list of a --table-dram-pass run (DRAM column)")
+    ap.add_argument("--table-from-json", default="",
+                    help="re-render the table from the JSON rows (stderr) of a --table run; no GPU")
+    ap.add_argument("--table-threads", type=int, default=os.cpu_count() or 1,
+                    help="--table-from-json: oracle threads of the recorded run, if the rows lack it")
+    ap.add_argument("--table-cpu", default="(not recorded)",
+                    help="--table-from-json: host CPU of the recorded run, if the rows lack it")
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)          # at least three untimed warm-up steps
     return a
@@ -1126,6 +1156,8 @@ def main(argv=None) -> int:
         return run_sweep(args)
     if args.suite:
         return run_suite(args)
+    if args.table_from_json:
+        return run_table_from_json(args)
     if args.table or args.table_dram_pass:
         return run_table(args)
     return run_ours(args)
