@@ -135,3 +135,19 @@ def test_table_rows_cover_every_config():
     assert {r[2] for r in rows if r[1] == 3} == {"twoshot", "twoshot_pull"}
     assert {r[5] for r in rows if r[1] == 5} == {1, 8, 64}
     assert set(bench._MAIN_KERNEL) >= {r[2] for r in rows}
+
+
+def test_format_table_flags_l2_served_rows():
+    base = {"label": "3", "algo": "twoshot", "dtype": "f32", "R": 8, "bytes_per_rank": 1 << 28,
+            "t_ms": 0.6, "algbw": 400.0, "compulsory_gbs": 7000.0, "parity": True,
+            "oracle_1t_ms": 200.0, "oracle_nt_ms": 16.0, "l2_resident": False}
+    rows = [dict(base, logical_gbs=7000.0, dram_gbs=6900.0),
+            dict(base, algo="twoshot_pull", logical_gbs=9600.0, dram_gbs=6600.0),
+            dict(base, label="1", logical_gbs=100.0, dram_gbs=50.0, l2_resident=True),
+            dict(base, label="5", algo="put_signal", logical_gbs=100.0, parity=False, oracle_nt_ms=None)]
+    md = bench.format_table(rows, 6789.0, "measured", 16, "cpu").splitlines()
+    assert "oracle 16-thread" in md[0]
+    assert "| 1.01 |" in md[2] and "L2-served" not in md[2]
+    assert "1.45 (L2-served)" in md[3]
+    assert "L2-resident (n/m)" in md[4]
+    assert "**MISMATCH**" in md[5] and "(compulsory)" in md[5]
