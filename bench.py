@@ -88,6 +88,14 @@ def recorded_traffic(R: int, S: int) -> float | None:
     return per_byte * S if int(t["R"]) == R else None
 
 
+def _size(nbytes: int) -> str:
+    """1 KiB, 64 MiB, 1 GiB ..."""
+    for unit, shift in (("GiB", 30), ("MiB", 20), ("KiB", 10)):
+        if nbytes >= 1 << shift and nbytes % (1 << shift) == 0:
+            return f"{nbytes >> shift} {unit}"
+    return f"{nbytes} B"
+
+
 def percentile(xs, q):
     xs = sorted(xs)
     if not xs:
@@ -501,9 +509,9 @@ def run_e2e(sm, send, recv, x, R, n, args, world, stream) -> dict:
 def run_secondary(sm, stream, x3, peak) -> list[dict]:
     """The other measured rows, each timed over >= 20 launches (CUDA events per launch on the
     library's stream, after 5 warm-ups) and checked against the oracle in the same run:
-    config 3 bf16 (two-shot, pull) and fp32 pull, config 2 one-shot and two-shot, config 5's
-    put + signal AllGather at 8 chunks per signal, and the AUTO crossover (64 / 256 KiB per rank).
-    x3: the config-3 fp32 inputs already on the host."""
+    R=8 x 128 MiB bf16 (two-shot, pull) and 256 MiB fp32 pull, R=8 x 64 MiB one-shot and two-shot, the
+    put + signal AllGather at 8 chunks per signal, and the AUTO crossover (64 to 512 KiB per rank).
+    x3: the R=8 x 256 MiB fp32 inputs already on the host."""
     import numpy as np
     import torch
 
@@ -552,11 +560,12 @@ def run_secondary(sm, stream, x3, peak) -> list[dict]:
             send.free()
             recv.free()
 
-    allreduce_rows("config3 bf16", wl.to_bf16_bits(x3), "bf16", ["twoshot", "twoshot_pull"])
-    allreduce_rows("config3 f32", x3, "f32", ["twoshot_pull"])
-    allreduce_rows("config2 f32", wl.config_inputs(2), "f32", ["oneshot", "twoshot"])
+    allreduce_rows("allreduce R=8 x 128 MiB bf16 U(-1,1)", wl.to_bf16_bits(x3), "bf16",
+                   ["twoshot", "twoshot_pull"])
+    allreduce_rows("allreduce R=8 x 256 MiB fp32 U(-1,1)", x3, "f32", ["twoshot_pull"])
+    allreduce_rows("allreduce R=8 x 64 MiB fp32 N(0,1)", wl.workload_inputs(2), "f32", ["oneshot", "twoshot"])
 
-    # config 5: put + signal AllGather, R=16 x 32 MiB, 64 KiB chunks, 8 chunks per signal
+    # put + signal AllGather, R=16 x 32 MiB, 64 KiB chunks, 8 chunks per signal
     c5 = wl.PUT_SIGNAL
     R, S, chunk, batch = c5["R"], c5["nbytes"], c5["chunk"], c5["batch"]
     xb = wl.random_bytes(5, R, S)
@@ -568,7 +577,7 @@ def run_secondary(sm, stream, x3, peak) -> list[dict]:
         ts = _time_launches(lambda: sm.sym_allgather(send, recv, S // 4, "f32", "put_signal", chunk,
                                                      batch), 20, stream)
         if sm.sym_stream_status() != sm.SYM_OK:
-            raise RuntimeError("config5: " + sm.sym_last_error())
+            raise RuntimeError("put + signal allgather: " + sm.sym_last_error())
         want, sig, cnt = oracle.put_signal_allgather(xb, chunk, batch)
         del xb
         ok = True
@@ -579,7 +588,8 @@ def run_secondary(sm, stream, x3, peak) -> list[dict]:
             ok &= bool(np.array_equal(out, want))
             ok &= all(sm.sym_signal_read(recv, p, q) == int(sig[p, q]) for q in range(R))
             ok &= sm.sym_counter_read(send, p, 0) == int(cnt[p])
-        row("config5 put_signal allgather", "put_signal (64 KiB chunks, 8 per signal)", "bytes", R, S,
+        row("put+signal allgather R=16 x 32 MiB random bytes", "put_signal (64 KiB chunks, 8 per signal)",
+            "bytes", R, S,
             ts, R * S + R * R * S, ok,
             "every rank's gathered bytes, all R*R signal counts and R counters equal the oracle's "
             "sequential put + signal model")
@@ -591,7 +601,7 @@ def run_secondary(sm, stream, x3, peak) -> list[dict]:
     points = []
     for nbytes in (64 << 10, 128 << 10, 256 << 10, 512 << 10):
         R, n = 8, nbytes // 4
-        x = wl.config_inputs(4, n=n)
+        x = wl.workload_inputs(4, n=n)
         send, recv = sm.Window(R, nbytes), sm.Window(R, nbytes)
         try:
             for r in range(R):
@@ -629,7 +639,7 @@ def run_secondary(sm, stream, x3, peak) -> list[dict]:
         finally:
             send.free()
             recv.free()
-    rows.append({"row": "config4 AUTO crossover", "R": 8, "dtype": "f32",
+    rows.append({"row": "allreduce R=8 fp32 N(0,1) AUTO crossover", "R": 8, "dtype": "f32",
                  "threshold": "SYM_ONESHOT_MAX_BYTES (128 KiB per rank)", "points": points,
                  "auto_over_best_max": max(p["auto_over_best"] for p in points),
                  "parity": all(p["parity"] for p in points),
@@ -792,13 +802,14 @@ def run_suite(args) -> int:
     def want(group):
         return not wanted or group in wanted
 
-    # AllReduce rows: configs 1-3 (fp32, bf16 where stated), every algorithm
+    # AllReduce rows: R=4 x 4 MiB, R=8 x 64 MiB and R=8 x 256 MiB (fp32, and 128 MiB bf16),
+    # every algorithm
     cases = [(1, "f32", ["oneshot", "twoshot", "twoshot_pull", "twoshot_split"]),
              (2, "f32", ["oneshot", "twoshot", "twoshot_pull", "twoshot_split"]),
              (3, "f32", ["twoshot", "twoshot_pull", "twoshot_split"]),
              (3, "bf16", ["twoshot", "twoshot_pull"])]
     for cfg, dt, algos in cases if want("allreduce") else []:
-        x = wl.config_inputs(cfg, n=wl.CONFIGS[cfg].count // scale)
+        x = wl.workload_inputs(cfg, n=wl.WORKLOADS[cfg].count // scale)
         if dt == "bf16":
             x = wl.to_bf16_bits(x)
         R, n = x.shape
@@ -812,19 +823,21 @@ def run_suite(args) -> int:
                                 iters_for(2 * R * S), stream)
             m = algo_bytes(algo, R, S)
             resident = 2 * R * S < (126 << 20)
-            report(f"allreduce config{cfg}", f"{algo} {dt}", ts, S, m["compulsory"], m["logical"],
+            report(f"allreduce R={R} x {_size(S)} {wl.WORKLOADS[cfg].dist}", f"{algo} {dt}", ts, S,
+                   m["compulsory"], m["logical"],
                    {"R": R, "bytes_per_rank": S, "l2_resident": resident})
             if resident:
                 # the same launches with L2 flushed before each one (cold column)
                 ts = timed(lambda: sm.sym_allreduce(send, recv, n, dt, "sum", algo),
                                     its(50), stream, flush)
-                report(f"allreduce config{cfg}", f"{algo} {dt} cold L2", ts, S, m["compulsory"],
+                report(f"allreduce R={R} x {_size(S)} {wl.WORKLOADS[cfg].dist}", f"{algo} {dt} cold L2",
+                       ts, S, m["compulsory"],
                        m["logical"], {"R": R, "bytes_per_rank": S, "l2_resident": False})
         send.free()
         recv.free()
         del x
 
-    # AllGather (copy, CE) and put+signal AllGather: config 5
+    # AllGather (copy, CE) and put+signal AllGather: R=16 x 32 MiB of random bytes
     if want("allgather") or want("put_signal"):
         cfg5 = wl.PUT_SIGNAL
         R, S = cfg5["R"], cfg5["nbytes"] // scale
@@ -838,13 +851,14 @@ def run_suite(args) -> int:
             ts = timed(lambda: sm.sym_allgather(send, recv, S // 4, "f32", algo), its(50),
                                 stream)
             kern = os.environ.get("SYM_ALLGATHER_KERNEL", "bulk") if algo == "copy" else "copy engines"
-            report("allgather config5", algo, ts, S, comp,
+            report(f"allgather R={R} x {_size(S)} bytes", algo, ts, S, comp,
                    extra={"R": R, "bytes_per_rank": S, "kernel": kern})
         nchunks = -(-S // cfg5["chunk"])
         for batch in (8, 1, 64) if want("put_signal") else ():
             ts = timed(lambda: sm.sym_allgather(send, recv, S // 4, "f32", "put_signal",
                                                          cfg5["chunk"], batch), its(50), stream)
-            report("put_signal allgather config5", f"chunk 64KiB, {batch} chunks/signal", ts, S, comp,
+            report(f"put_signal allgather R={R} x {_size(S)} bytes", f"chunk 64KiB, {batch} chunks/signal",
+                   ts, S, comp,
                    extra={"R": R, "bytes_per_rank": S, "signals_per_pair": -(-nchunks // batch)})
         send.free()
         recv.free()
@@ -864,9 +878,9 @@ def run_suite(args) -> int:
         send.free()
         recv.free()
 
-    # fused producer + AllReduce: config-3 size
+    # fused producer + AllReduce: R=8 x 256 MiB fp32
     if want("fused"):
-        x = wl.config_inputs(3, n=wl.CONFIGS[3].count // scale)
+        x = wl.workload_inputs(3, n=wl.WORKLOADS[3].count // scale)
         R, n = x.shape
         S = n * 4
         win_in, send, recv = sm.Window(R, S), sm.Window(R, S), sm.Window(R, S)
@@ -907,25 +921,25 @@ _MAIN_KERNEL = {"oneshot": "k_oneshot", "twoshot": "k_twoshot_st", "twoshot_pull
 
 
 def table_rows():
-    """(label, config index, algo, dtype, count or bytes, extra) of every results-table row."""
+    """(label, workload index, algo, dtype, count or bytes, extra) of every results-table row."""
     rows = []
     for dist in ("rankfill", "normal"):
         for algo in ("oneshot", "twoshot"):
-            rows.append((f"1 ({'rank fill' if dist == 'rankfill' else 'N(0,1)'})", 1, algo, "f32",
-                         1 << 20, dist))
+            rows.append((f"R=4 × 4 MiB, {'rank fill' if dist == 'rankfill' else 'N(0,1)'}", 1, algo,
+                         "f32", 1 << 20, dist))
     for algo in ("oneshot", "twoshot", "twoshot_pull"):
-        rows.append(("2", 2, algo, "f32", 1 << 24, None))
+        rows.append(("R=8 × 64 MiB, N(0,1)", 2, algo, "f32", 1 << 24, None))
     for dt in ("f32", "bf16"):
         for algo in ("twoshot", "twoshot_pull"):
-            rows.append(("3", 3, algo, dt, 1 << 26, None))
+            rows.append((f"R=8 × {_size((1 << 26) * (4 if dt == 'f32' else 2))}, U(-1,1)", 3, algo, dt,
+                         1 << 26, None))
     for k in range(11):
         nbytes = 1024 * 4 ** k
-        size = f"{nbytes >> 10} KiB" if nbytes < (1 << 20) else (
-            f"{nbytes >> 20} MiB" if nbytes < (1 << 30) else f"{nbytes >> 30} GiB")
         for algo in ("oneshot", "twoshot"):
-            rows.append((f"4: {size}/rank", 4, algo, "f32", nbytes // 4, None))
+            rows.append((f"R=8 × {_size(nbytes)}, N(0,1) (sweep)", 4, algo, "f32", nbytes // 4, None))
     for batch in (8, 1, 64):
-        rows.append((f"5 (64 KiB chunks, {batch}/signal)", 5, "put_signal", "bytes", 32 << 20, batch))
+        rows.append((f"R=16 × 32 MiB bytes, 64 KiB chunks, {batch}/signal", 5, "put_signal", "bytes",
+                     32 << 20, batch))
     return rows
 
 
@@ -934,7 +948,7 @@ def _table_inputs(cfg, dt, n, extra):
 
     if cfg == 5:
         return wl.random_bytes(5, wl.PUT_SIGNAL["R"], n)
-    x = wl.config_inputs(cfg, n=n, dist=extra) if cfg != 4 else wl.config_inputs(4, n=n)
+    x = wl.workload_inputs(cfg, n=n, dist=extra) if cfg != 4 else wl.workload_inputs(4, n=n)
     return wl.to_bf16_bits(x) if dt == "bf16" else x
 
 
@@ -1066,7 +1080,7 @@ def format_table(rows: list[dict], peak: float, peak_kind: str, nthr: int, cpu: 
     """Markdown of the results table from its JSON rows (as run_table writes them to stderr).
     A row is flagged L2-served when its logical bytes exceed the DRAM bytes by more than 10 %:
     repeated reads of the same lines came from L2, not HBM."""
-    lines = [f"| Config | Algo | dtype | t median (ms) | algbw GB/s | logical GB/s | compulsory GB/s "
+    lines = [f"| Workload | Algo | dtype | t median (ms) | algbw GB/s | logical GB/s | compulsory GB/s "
              f"| HBM GB/s (ncu DRAM bytes / t) | % of measured peak | logical / DRAM | parity "
              f"| oracle 1-thread (ms) | oracle {nthr}-thread (ms) |",
              "|---|---|---|---|---|---|---|---|---|---|---|---|---|"]
@@ -1118,7 +1132,8 @@ def parse(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
-                    help="skip the other rows (config 3 bf16, config 2, config 5, AUTO crossover)")
+                    help="skip the other rows (bf16 and pull at R=8 x 256 MiB, R=8 x 64 MiB, "
+                         "put + signal AllGather, AUTO crossover)")
     ap.add_argument("--sweep", action="store_true",
                     help="message-size sweep of every algorithm instead of the contract line")
     ap.add_argument("--sweep-max", type=int, default=1 << 30)

@@ -905,7 +905,7 @@ sym_status_t launch_algo(sym_algo_t algo, ArArgs& a, sym_win_t recv, cudaStream_
                 break;
             }
             // two 16 KiB tiles per item, gathers 4 grid waves behind: measured best
-            // of 1/2/4/8 tiles x 2/4/8 waves (config 3 fp32 0.721 -> 0.685 ms)
+            // of 1/2/4/8 tiles x 2/4/8 waves (R = 8 x 256 MiB fp32: 0.721 -> 0.685 ms)
             a.group = kPullGroup;
             size_t slots = (size_t)a.R * a.R * ceil_div(a.tiles_per_chunk, (size_t)a.group);
             size_t grid = std::min(std::max(slots, (size_t)1), cap);

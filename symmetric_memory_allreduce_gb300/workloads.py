@@ -6,7 +6,7 @@ here, so both sides see identical bytes.
 
 Recipe (host numpy, ``Generator(PCG64(seed))``):
 
-* per-rank seed = ``20261202 + 1000 * config + rank``;
+* per-rank seed = ``20261202 + 1000 * workload + rank`` (workloads numbered 1-5 as below);
 * N(0,1) values: ``standard_normal(n, dtype=float32)``;
 * U(-1,1) values: ``2 * random(n, dtype=float32) - 1`` (float32 arithmetic);
 * "rank fill": every element of rank ``r`` is ``float(r)``;
@@ -32,27 +32,27 @@ MiB = 1024 * KiB
 GiB = 1024 * MiB
 
 
-def rank_seed(config: int, rank: int) -> int:
-    return SEED_BASE + 1000 * int(config) + int(rank)
+def rank_seed(workload: int, rank: int) -> int:
+    return SEED_BASE + 1000 * int(workload) + int(rank)
 
 
-def _gen(config: int, rank: int) -> np.random.Generator:
-    return np.random.Generator(np.random.PCG64(rank_seed(config, rank)))
+def _gen(workload: int, rank: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(rank_seed(workload, rank)))
 
 
-def normal_f32(config: int, R: int, n: int) -> np.ndarray:
+def normal_f32(workload: int, R: int, n: int) -> np.ndarray:
     """(R, n) float32, rank r drawn N(0,1) from its own seed."""
     out = np.empty((R, n), np.float32)
     for r in range(R):
-        out[r] = _gen(config, r).standard_normal(n, dtype=np.float32)
+        out[r] = _gen(workload, r).standard_normal(n, dtype=np.float32)
     return out
 
 
-def uniform_f32(config: int, R: int, n: int) -> np.ndarray:
+def uniform_f32(workload: int, R: int, n: int) -> np.ndarray:
     """(R, n) float32, rank r drawn U(-1,1) from its own seed."""
     out = np.empty((R, n), np.float32)
     for r in range(R):
-        u = _gen(config, r).random(n, dtype=np.float32)
+        u = _gen(workload, r).random(n, dtype=np.float32)
         np.multiply(u, np.float32(2.0), out=u)
         np.subtract(u, np.float32(1.0), out=u)
         out[r] = u
@@ -64,10 +64,10 @@ def rank_fill_f32(R: int, n: int) -> np.ndarray:
     return np.repeat(np.arange(R, dtype=np.float32)[:, None], n, axis=1)
 
 
-def random_bytes(config: int, R: int, nbytes: int) -> np.ndarray:
+def random_bytes(workload: int, R: int, nbytes: int) -> np.ndarray:
     out = np.empty((R, nbytes), np.uint8)
     for r in range(R):
-        out[r] = _gen(config, r).integers(0, 256, nbytes, dtype=np.uint8)
+        out[r] = _gen(workload, r).integers(0, 256, nbytes, dtype=np.uint8)
     return out
 
 
@@ -80,7 +80,7 @@ def to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
 
 @dataclass(frozen=True)
-class AllReduceConfig:
+class AllReduceWorkload:
     index: int
     name: str
     R: int
@@ -89,12 +89,12 @@ class AllReduceConfig:
     algos: tuple
 
 
-CONFIGS = {
-    1: AllReduceConfig(1, "allreduce R=4 N=1048576 fp32 (rank fill, then N(0,1))", 4, 1 << 20,
+WORKLOADS = {
+    1: AllReduceWorkload(1, "allreduce R=4 N=1048576 fp32 (rank fill, then N(0,1))", 4, 1 << 20,
                        "normal", ("oneshot",)),
-    2: AllReduceConfig(2, "allreduce R=8 N=16777216 fp32 N(0,1)", 8, 1 << 24, "normal",
+    2: AllReduceWorkload(2, "allreduce R=8 N=16777216 fp32 N(0,1)", 8, 1 << 24, "normal",
                        ("oneshot", "twoshot")),
-    3: AllReduceConfig(3, "allreduce R=8 N=67108864 (256 MiB fp32 / 128 MiB bf16) U(-1,1)", 8,
+    3: AllReduceWorkload(3, "allreduce R=8 N=67108864 (256 MiB fp32 / 128 MiB bf16) U(-1,1)", 8,
                        1 << 26, "uniform", ("twoshot",)),
 }
 
@@ -105,14 +105,14 @@ SWEEP_BYTES = [KiB * 4 ** k for k in range(11)]
 PUT_SIGNAL = dict(R=16, nbytes=32 * MiB, chunk=64 * KiB, batch=8)
 
 
-def config_inputs(index: int, n: int | None = None, dist: str | None = None) -> np.ndarray:
-    """Inputs of AllReduce config ``index`` (optionally truncated to ``n`` elements per rank)."""
+def workload_inputs(index: int, n: int | None = None, dist: str | None = None) -> np.ndarray:
+    """Inputs of AllReduce workload ``index`` (optionally truncated to ``n`` elements per rank)."""
     if index == 4:
         R, dist = 8, dist or "normal"
         if n is None:
             raise ValueError("the sweep needs an explicit element count")
     else:
-        c = CONFIGS[index]
+        c = WORKLOADS[index]
         R, n, dist = c.R, (c.count if n is None else n), (dist or c.dist)
     if dist == "normal":
         return normal_f32(index, R, n)

@@ -47,7 +47,7 @@ def test_worked_example_rankfill(symar, oracle):
     """4 ranks of 1,048,576 floats filled with their rank: every element 6.0."""
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
-    x = wl.config_inputs(1, dist="rankfill")
+    x = wl.workload_inputs(1, dist="rankfill")
     for algo in ALGOS:
         y = _run(symar, x, "f32", algo)
         assert np.all(np.abs(y - 6.0) <= 0.001)
@@ -55,10 +55,10 @@ def test_worked_example_rankfill(symar, oracle):
 
 
 @pytest.mark.parametrize("algo", ALGOS)
-def test_config1_normal(symar, oracle, algo):
+def test_rank4_normal(symar, oracle, algo):
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
-    x = wl.config_inputs(1, dist="normal")
+    x = wl.workload_inputs(1, dist="normal")
     _check_f32(_run(symar, x, "f32", algo), oracle.allreduce_sum_f32(x))
 
 
@@ -248,7 +248,7 @@ def test_registered_torch_memory(symar, oracle):
         recv.free()
 
 
-# ---------------------------------------------------------------- full-size configs
+# ---------------------------------------------------------------- full-size workloads
 
 def _full(symar, oracle, x, dtype, algos):
     R, n = x.shape
@@ -277,34 +277,34 @@ def _full(symar, oracle, x, dtype, algos):
         recv.free()
 
 
-def test_config2_full(symar, oracle):
+def test_full_R8x64MiB(symar, oracle):
     """R=8 x 16,777,216 fp32 N(0,1): one-shot and two-shot, every rank bit-exact."""
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
-    _full(symar, oracle, wl.config_inputs(2), "f32", ALGOS)
+    _full(symar, oracle, wl.workload_inputs(2), "f32", ALGOS)
 
 
-def test_config3_full_f32(symar, oracle):
+def test_full_R8x256MiB_f32(symar, oracle):
     """R=8 x 67,108,864 fp32 U(-1,1) (256 MiB per rank), two-shot forms."""
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
-    _full(symar, oracle, wl.config_inputs(3), "f32", ["twoshot", "twoshot_pull", "twoshot_split", "auto"])
+    _full(symar, oracle, wl.workload_inputs(3), "f32", ["twoshot", "twoshot_pull", "twoshot_split", "auto"])
 
 
-def test_config3_full_bf16(symar, oracle):
+def test_full_R8x128MiB_bf16(symar, oracle):
     """The same draws rounded to bf16 (128 MiB per rank), fp32 accumulation."""
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
-    xb = wl.to_bf16_bits(wl.config_inputs(3))
+    xb = wl.to_bf16_bits(wl.workload_inputs(3))
     _full(symar, oracle, xb, "bf16", ["twoshot", "twoshot_pull", "twoshot_split"])
 
 
-def test_config3_full_f16(symar, oracle):
+def test_full_R8x128MiB_f16(symar, oracle):
     """The same draws rounded to fp16 (128 MiB per rank): fp32 accumulation in rank
     order, one rounding, bit-exact on every rank for the two-shot forms."""
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
-    x = np.ascontiguousarray(wl.config_inputs(3).astype(np.float16).view(np.uint16))
+    x = np.ascontiguousarray(wl.workload_inputs(3).astype(np.float16).view(np.uint16))
     R, n = x.shape
     want = oracle.allreduce(x, "f16", "sum")
     send, recv = symar.Window(R, n * 2), symar.Window(R, n * 2)
@@ -324,22 +324,22 @@ def test_config3_full_f16(symar, oracle):
 
 
 @pytest.mark.parametrize("nbytes", [1024 * 4 ** k for k in range(10)])
-def test_config4_sweep(symar, oracle, nbytes):
+def test_size_sweep(symar, oracle, nbytes):
     """R=8, 1 KiB .. 256 MiB per rank, fp32 N(0,1), every algorithm and AUTO."""
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
-    x = wl.config_inputs(4, n=nbytes // 4)
+    x = wl.workload_inputs(4, n=nbytes // 4)
     _full(symar, oracle, x, "f32", ALGOS + ["auto"])
 
 
-def test_config4_sweep_1gib_full(symar, oracle):
+def test_size_sweep_1gib_full(symar, oracle):
     """The 1 GiB-per-rank point, every element of every rank against the oracle
     ([SYMEX] Example 1 step 6 checks every element), for every algorithm and AUTO.
     Host memory: the 8 GiB of inputs, the 1 GiB oracle result and one rank's output."""
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
     R, n = 8, (1 << 30) // 4
-    x = wl.config_inputs(4, n=n)
+    x = wl.workload_inputs(4, n=n)
     send, recv = symar.Window(R, n * 4), symar.Window(R, n * 4)
     try:
         upload(send, x)

@@ -41,10 +41,10 @@ def test_scale_allreduce_closed_form(symar):
 
 
 def test_scale_allreduce_full_size_repeat(symar, oracle):
-    """R=8 x 16M fp32 (config-2 size), three calls on the same windows (epoch flags)."""
+    """R=8 x 16M fp32 (64 MiB per rank), three calls on the same windows (epoch flags)."""
     from symmetric_memory_allreduce_gb300 import workloads as wl
 
-    a = wl.config_inputs(2)
+    a = wl.workload_inputs(2)
     R, n = a.shape
     alpha = np.linspace(0.5, 2.0, R).astype(np.float32)
     s_w, y_w = oracle.scale_allreduce(a, alpha)

@@ -267,7 +267,7 @@ def test_put_signal_model_closed_forms(oracle, R, S, chunk, B):
     assert np.all(cnt == R * nchunks)
 
 
-def test_put_signal_model_config5_counts(oracle):
+def test_put_signal_model_R16x32MiB_counts(oracle):
     """R=16, 32 MiB in 64 KiB chunks (512 chunks), 8 chunks per signal -> 64 signals per pair."""
     R, chunk, B = 16, 64 << 10, 8
     S = 2 * chunk * B + chunk // 2          # small stand-in with a short last chunk

@@ -63,7 +63,7 @@ def test_allgather_random_bytes(symar, oracle, R, S, algo):
 
 
 @pytest.mark.parametrize("batch", [8, 1, 64])
-def test_config5_put_signal_full(symar, oracle, batch):
+def test_put_signal_full_R16x32MiB(symar, oracle, batch):
     """R=16, 32 MiB per rank, 64 KiB chunks: bytes, signal counts, counters, and the
     prefix-visibility check made by the receivers while the senders run."""
     import torch

@@ -46,7 +46,7 @@ for R in (2, 3, 8, 16, 64):
                 a.free()
                 if not in_place:
                     b.free()
-x = wl.config_inputs(3)
+x = wl.workload_inputs(3)
 R, n = x.shape
 a, b = sm.Window(R, n * 4), sm.Window(R, n * 4)
 upload(a, x)

@@ -38,7 +38,7 @@ for R in (1, 2, 3, 8, 16):
                 a.free()
                 if not in_place:
                     b.free()
-x = wl.config_inputs(3)
+x = wl.workload_inputs(3)
 R, n = x.shape
 a, b = sm.Window(R, n * 4), sm.Window(R, n * 4)
 upload(a, x)
