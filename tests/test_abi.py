@@ -97,3 +97,23 @@ def test_binding_mirrors_header_enums():
             assert getattr(_binding, name) == val, name
     for key, code in _binding.ALGOS.items():
         assert v["SYM_ALGO_" + key.upper()] == code
+
+
+def test_binding_signatures_match_header_arity():
+    """Every declared entry point takes as many arguments as the ctypes binding passes."""
+    import re
+
+    from symmetric_memory_allreduce_gb300 import _binding
+
+    body = open(_binding.HEADER).read()
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)          # drop comments
+    decls = re.findall(r"\b(sym_\w+)\s*\(([^;{]*?)\)\s*;", body, flags=re.S)
+    seen = 0
+    for name, params in decls:
+        if name not in _binding._SIGS:
+            continue
+        params = params.strip()
+        arity = 0 if params in ("", "void") else params.count(",") + 1
+        assert arity == len(_binding._SIGS[name][0]), name
+        seen += 1
+    assert seen == len(_binding.header_symbols())
